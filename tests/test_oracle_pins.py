@@ -1,0 +1,160 @@
+"""The oracle against its pins, and planted mistakes against the pins.
+
+A pin only counts if a plausible mistake in the oracle would fail it, so the
+second half plants such mistakes in a copy of the oracle (on the CPU) and
+checks that at least one pin rejects each.
+"""
+from __future__ import annotations
+
+import importlib.util
+import math
+import sys
+
+import numpy as np
+import pytest
+
+import oracle.mel_oracle as real_oracle
+from tests import oracle_pins as pins
+
+
+@pytest.mark.parametrize("check", pins.ALL_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(check):
+    check(real_oracle)
+
+
+def _fresh_oracle():
+    spec = importlib.util.spec_from_file_location("oracle_mutant", real_oracle.__file__)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _symmetric_hann(o):
+    def hann(win_length, n_fft):
+        n = np.arange(win_length, dtype=np.float64)
+        w = 0.5 - 0.5 * np.cos(2.0 * math.pi * n / (win_length - 1))
+        out = np.zeros(n_fft)
+        left = (n_fft - win_length) // 2
+        out[left : left + win_length] = w
+        return out
+
+    o.hann_periodic = hann
+
+
+def _edge_repeating_pad(o):
+    def pad_fn(x, pad):
+        return np.concatenate([x[..., :pad][..., ::-1], x, x[..., -pad:][..., ::-1]], axis=-1)
+
+    o.reflect_pad = pad_fn
+
+
+def _off_by_one_frames(o):
+    o.n_frames = lambda T, hop: (T + hop - 1) // hop
+
+
+def _dft_wrong_sign_angle_index(o):
+    orig = o.dft_onesided
+
+    def dft(y):
+        N = y.shape[-1]
+        n = np.arange(N)[:, None]
+        k = np.arange(N // 2 + 1)[None, :]
+        ang = 2.0 * math.pi * ((k + 1) * n % N) / N  # transposed/shifted index
+        return y @ np.cos(ang) - 1j * (y @ np.sin(ang))
+
+    o.dft_onesided = dft
+    del orig
+
+
+def _falling_edge_foot(o):
+    orig = o.mel_filterbank
+
+    def fb(n_fft, sr, n_mels, f_min, f_max, scale="htk", norm=None):
+        fk = o.bin_frequencies(n_fft, sr)[None, :]
+        v = o.filter_vertices(f_min, f_max, n_mels, scale)
+        lo, mid, hi = v[:-2, None], v[1:-1, None], v[2:, None]
+        rising = (fk - lo) / (mid - lo)
+        falling = (hi - fk) / (hi - lo)  # wrong denominator
+        F = np.maximum(0.0, np.minimum(rising, falling))
+        if norm == "slaney":
+            F = F * (2.0 / (v[2:] - v[:-2]))[:, None]
+        return F
+
+    o.mel_filterbank = fb
+    del orig
+
+
+def _slaney_norm_base(o):
+    orig = o.mel_filterbank
+
+    def fb(n_fft, sr, n_mels, f_min, f_max, scale="htk", norm=None):
+        F = orig(n_fft, sr, n_mels, f_min, f_max, scale, None)
+        if norm == "slaney":
+            v = o.filter_vertices(f_min, f_max, n_mels, scale)
+            F = F * (2.0 / (v[1:-1] - v[:-2]))[:, None]  # half the base
+        return F
+
+    o.mel_filterbank = fb
+
+
+def _htk_natural_log(o):
+    orig = o.hz_to_mel
+
+    def h2m(f, scale):
+        if scale == "htk":
+            return 2595.0 * np.log(1.0 + np.asarray(f, dtype=np.float64) / 700.0)
+        return orig(f, scale)
+
+    o.hz_to_mel = h2m
+
+
+def _int16_scale(o):
+    orig = o.to_float64
+
+    def conv(x):
+        x = np.asarray(x)
+        if x.dtype == np.int16:
+            return x.astype(np.float64) / 32767.0
+        return orig(x)
+
+    o.to_float64 = conv
+
+
+def _power_half(o):
+    orig = o.spectral_power
+
+    def sp(X, power):
+        return orig(X, power) * (0.5 if power == 2.0 else 1.0)
+
+    o.spectral_power = sp
+
+
+MUTANTS = [
+    _symmetric_hann,
+    _edge_repeating_pad,
+    _off_by_one_frames,
+    _dft_wrong_sign_angle_index,
+    _falling_edge_foot,
+    _slaney_norm_base,
+    _htk_natural_log,
+    _int16_scale,
+    _power_half,
+]
+
+
+@pytest.mark.parametrize("mutate", MUTANTS, ids=lambda m: m.__name__.strip("_"))
+def test_pins_catch_planted_mistake(mutate):
+    o = _fresh_oracle()
+    mutate(o)
+    failed = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(o)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(check.__name__)
+    assert failed, f"no pin caught the planted mistake {mutate.__name__}"
+
+
+def test_mutants_do_not_leak():
+    assert "oracle_mutant" not in sys.modules or sys.modules["oracle_mutant"] is not real_oracle
+    pins.check_bin_centre_cosine(real_oracle)
