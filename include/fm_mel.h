@@ -1,0 +1,193 @@
+/*
+ * fm_mel.h -- C ABI of the GB300 (sm_103a) batched mel spectrogram.
+ *
+ * The operation is torchaudio's MelSpectrogram as the flashmel 0.1.0 page
+ * states it (README, "Usage" and "How it works"; filters.py, make_window and
+ * pack_fbank):
+ *
+ *   out[b, m, t] = sum_k F[m, k] * |X_{b,t}[k]|^power
+ *   X_{b,t}[k]   = sum_{n < n_fft} xp_b[t*hop + n] * w[n] * exp(-2 pi i k n / n_fft)
+ *
+ * with xp_b the signal reflect-padded by n_fft/2 on both sides (centre=True,
+ * pad_mode="reflect"), w the periodic Hann window of win_length samples
+ * zero-padded and centred to n_fft, k = 0 .. n_fft/2, t = 0 .. T/hop, and F
+ * the triangular mel filterbank (HTK or Slaney mel scale, optional Slaney
+ * area norm) over bins at frequency k*sr/n_fft.
+ *
+ * Conventions for every call:
+ *   - Errors are returned as fm_status; nothing is thrown or printed, and a
+ *     failing call has no side effects.
+ *   - "device pointer" means memory the current CUDA device can address
+ *     (cudaMalloc / torch CUDA tensors); "host pointer" means CPU memory.
+ *   - All arrays are dense and row-major.
+ *
+ * This header needs no CUDA header: fm_stream_t is ABI-identical to
+ * cudaStream_t / CUstream (a pointer to the opaque CUstream_st); pass NULL
+ * for the legacy default stream.
+ */
+#ifndef FM_MEL_H
+#define FM_MEL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fm_stream_t;
+typedef struct fm_plan fm_plan; /* opaque; owns its device tables */
+
+typedef enum {
+  FM_OK = 0,
+  FM_ERR_INVALID_ARG = 1,    /* a NULL pointer, a size or a parameter out of range */
+  FM_ERR_UNSUPPORTED = 2,    /* valid for torchaudio, but not built here (see fm_plan_create) */
+  FM_ERR_CUDA = 3,           /* a CUDA runtime call failed (no device, launch failure, ...) */
+  FM_ERR_OOM = 4,            /* device or host allocation failed */
+  FM_ERR_KERNEL_TIMEOUT = 5  /* a bounded device-side wait gave up (reported by fm_plan_poll_error) */
+} fm_status;
+
+typedef enum { FM_MEL_HTK = 0, FM_MEL_SLANEY = 1 } fm_mel_scale;
+typedef enum { FM_NORM_NONE = 0, FM_NORM_SLANEY = 1 } fm_norm;
+typedef enum { FM_F32 = 0, FM_I16 = 1, FM_F16 = 2 } fm_dtype;
+
+/*
+ * fm_plan_create -- validate the transform parameters and build its tables.
+ *
+ * flashmel README "Usage" (torchaudio arguments, input dtype f32 or int16
+ * PCM scaled by 1/32768, output dtype f32 or f16) and "How it works" (window
+ * and sparse filterbank built once on the host); filters.py make_window /
+ * pack_fbank. f16 input (computed in fp32) is this library's addition.
+ *
+ *   out        : receives the new plan (host pointer to a pointer). Set to
+ *                NULL on failure.
+ *   sr         : sample rate in Hz, > 0.
+ *   n_fft      : DFT size. Supported: 400 and the powers of two 64 .. 2048.
+ *   hop        : frame advance in samples, > 0 and even.
+ *   win_length : Hann length, 1 .. n_fft; 0 means n_fft.
+ *   n_mels     : number of mel filters, 1 .. 256.
+ *   f_min      : lowest filter edge in Hz, >= 0.
+ *   f_max      : highest filter edge in Hz, f_min < f_max <= sr/2;
+ *                f_max <= 0 means sr/2.
+ *   power      : exponent on |X|, finite and > 0 (2 = power, 1 = magnitude).
+ *   mel_scale  : FM_MEL_HTK or FM_MEL_SLANEY.
+ *   norm       : FM_NORM_NONE or FM_NORM_SLANEY (filter m scaled by
+ *                2 / (f[m+2] - f[m]), i.e. unit area).
+ *   in_dtype   : storage type of the input samples (FM_F32, FM_I16, FM_F16).
+ *   out_dtype  : FM_F32 or FM_F16 (round-to-nearest-even at the store;
+ *                accumulation is always fp32).
+ *
+ * Builds the window, the DFT twiddles and the per-filter CSR (start, length,
+ * offset, weights) in float64 on the host, rounds them to fp32 and copies them
+ * to memory on the current CUDA device, which the plan owns until
+ * fm_plan_destroy. The plan is read-only afterwards: it may be used from
+ * several host threads and streams at once, on the device it was created on.
+ *
+ * Errors: FM_ERR_INVALID_ARG (out NULL or a parameter out of range, including
+ * out_dtype == FM_I16); FM_ERR_UNSUPPORTED (n_fft not in the supported set,
+ * n_mels > 256, odd hop); FM_ERR_CUDA (no usable device); FM_ERR_OOM.
+ */
+fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, int win_length, int n_mels,
+                         double f_min, double f_max, double power, fm_mel_scale mel_scale,
+                         fm_norm norm, fm_dtype in_dtype, fm_dtype out_dtype);
+
+/* fm_plan_destroy -- free the plan's device tables. NULL is accepted (no-op).
+ * Work already queued with the plan must have finished (e.g. synchronise the
+ * streams first). Returns FM_OK, or FM_ERR_CUDA if freeing failed. */
+fm_status fm_plan_destroy(fm_plan* plan);
+
+/* fm_n_frames -- frames per signal for T samples with centre padding:
+ * 1 + floor(T / hop) (torch.stft, center=True). Returns -1 if plan is NULL or
+ * T < 0. */
+int64_t fm_n_frames(const fm_plan* plan, int64_t T);
+
+/*
+ * fm_mel_forward -- the whole path in one kernel launch, asynchronously on
+ * `stream` (README "How it works": pad, frame, window, R2C DFT, |X|^power and
+ * the sparse mel projection fused; launched on the caller's stream).
+ *
+ *   d_in   : device pointer, [B][T] samples of the plan's in_dtype,
+ *            contiguous, any alignment of the element type. Not modified.
+ *   B      : number of signals, >= 0. B == 0 returns FM_OK and does nothing
+ *            (d_in / d_out may then be NULL).
+ *   T      : samples per signal; must exceed n_fft/2 (a reflect pad cannot be
+ *            longer than the signal).
+ *   d_out  : device pointer, [B][n_mels][fm_n_frames(T)] of the plan's
+ *            out_dtype, contiguous, element-aligned; fully overwritten. Must
+ *            not overlap d_in.
+ *   stream : the CUDA stream to run on (NULL = legacy default stream).
+ *
+ * Allocates nothing and does not synchronise. Both buffers are owned by the
+ * caller and must stay valid until the stream reaches this work.
+ * Errors: FM_ERR_INVALID_ARG (NULL plan or pointer with B > 0, B < 0,
+ * T <= n_fft/2, B*T or the output size beyond 2^62 elements); FM_ERR_CUDA
+ * (launch failed, or called on another device than the plan's).
+ */
+fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64_t B, int64_t T, void* d_out,
+                         fm_stream_t stream);
+
+/*
+ * fm_mel_forward_host -- fm_mel_forward for inputs and outputs in host memory.
+ *
+ * Queues on `stream`: a copy of h_in [B][T] into d_in_scratch, the kernel,
+ * and a copy of d_out_scratch into h_out [B][n_mels][n_frames]. The caller
+ * supplies both device buffers (at least B*T and B*n_mels*n_frames elements)
+ * so the call allocates nothing; pinned host memory makes the copies
+ * asynchronous. The caller synchronises `stream` before reading h_out.
+ * Errors: as fm_mel_forward, plus FM_ERR_INVALID_ARG for NULL buffers.
+ */
+fm_status fm_mel_forward_host(const fm_plan* plan, const void* h_in, int64_t B, int64_t T,
+                              void* h_out, void* d_in_scratch, void* d_out_scratch,
+                              fm_stream_t stream);
+
+/*
+ * fm_mel_filterbank_csr -- the plan's filterbank, computed on the host only
+ * (no CUDA call), for inspection and tests.
+ *
+ * filters.py pack_fbank: a triangular filter has contiguous support, so row
+ * m is stored as start[m], len[m] and len[m] weights beginning at off[m] in
+ * `weights` (off[m+1] = off[m] + len[m]). An empty filter has len 0.
+ *
+ *   start, len : host int32 arrays of n_mels entries (may be NULL to query).
+ *   off        : host int32 array of n_mels + 1 entries (may be NULL).
+ *   weights    : host float array with room for *nnz floats (may be NULL).
+ *   nnz        : in: capacity of `weights`; out: entries needed. Required.
+ * Returns FM_ERR_INVALID_ARG for bad parameters (same rules as
+ * fm_plan_create) or if weights is non-NULL and its capacity is too small.
+ */
+fm_status fm_mel_filterbank_csr(int sr, int n_fft, int n_mels, double f_min, double f_max,
+                                fm_mel_scale mel_scale, fm_norm norm, int32_t* start, int32_t* len,
+                                int32_t* off, float* weights, int64_t* nnz);
+
+/* Facts about a plan, for sizing buffers and computing roofline figures. */
+typedef struct {
+  int n_fft, hop, win_length, n_mels, n_freqs;
+  int in_dtype, out_dtype;
+  int64_t nnz;            /* filterbank non-zeros */
+  int frames_per_tile;    /* frames one CTA processes per tile */
+  int threads_per_block;  /* CTA size of the kernel */
+  int blocks_per_sm;      /* resident CTAs per SM (occupancy) */
+  int grid_limit;         /* persistent grid size = SMs x blocks_per_sm */
+  int smem_bytes;         /* dynamic shared memory per CTA */
+  int device;             /* CUDA device the plan lives on */
+} fm_plan_info;
+
+/* fm_plan_get_info -- fill *info. FM_ERR_INVALID_ARG on NULL arguments. */
+fm_status fm_plan_get_info(const fm_plan* plan, fm_plan_info* info);
+
+/*
+ * fm_plan_poll_error -- read and clear the plan's device error word
+ * (synchronising the plan's device). Kernels that wait on a device-side
+ * barrier give up after a bounded number of polls, record FM_ERR_KERNEL_TIMEOUT
+ * there and return instead of hanging. Returns FM_OK if nothing was recorded.
+ */
+fm_status fm_plan_poll_error(const fm_plan* plan);
+
+/* fm_status_string -- a static, human-readable name for a status code. */
+const char* fm_status_string(fm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FM_MEL_H */

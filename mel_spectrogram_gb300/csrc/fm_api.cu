@@ -1,0 +1,297 @@
+// C-ABI layer: plan creation (validation, host tables, device upload) and the
+// launch of the fused kernel. See include/fm_mel.h for the contract.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "fm_host.h"
+#include "fm_internal.h"
+#include "fm_mel.h"
+
+namespace fm {
+extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant512, kVariant1024,
+    kVariant2048;
+
+const Variant* find_variant(int n_fft) {
+  static const Variant* all[] = {&kVariant64,  &kVariant128,  &kVariant256, &kVariant400,
+                                 &kVariant512, &kVariant1024, &kVariant2048};
+  for (const Variant* v : all)
+    if (v->n_fft == n_fft) return v;
+  return nullptr;
+}
+}  // namespace fm
+
+struct fm_plan {
+  int device;
+  int sr, n_fft, hop, win_length, n_mels;
+  double f_min, f_max, power;
+  int mel_scale, norm, in_dtype, out_dtype, power_mode;
+  const fm::Variant* var;
+  int nnz;
+  size_t smem;
+  int blocks_per_sm, grid_limit, num_sms;
+  void* dmem;
+  float* window;
+  float2* tw_half;
+  float2* tw_full;
+  int* mel_start;
+  int* mel_len;
+  int* mel_off;
+  float* mel_w;
+  unsigned* err;
+};
+
+namespace {
+
+int dtype_size(int dt) { return dt == FM_F32 ? 4 : 2; }
+
+fm_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return FM_OK;
+  if (e == cudaErrorMemoryAllocation) return FM_ERR_OOM;
+  return FM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, int win_length, int n_mels,
+                                    double f_min, double f_max, double power, fm_mel_scale mel_scale,
+                                    fm_norm norm, fm_dtype in_dtype, fm_dtype out_dtype) {
+  if (out == nullptr) return FM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (win_length == 0) win_length = n_fft;
+  if (sr <= 0 || n_fft <= 0 || hop <= 0 || n_mels <= 0) return FM_ERR_INVALID_ARG;
+  if (win_length < 0 || win_length > n_fft) return FM_ERR_INVALID_ARG;
+  if (!std::isfinite(power) || !(power > 0.0)) return FM_ERR_INVALID_ARG;
+  if (in_dtype != FM_F32 && in_dtype != FM_I16 && in_dtype != FM_F16) return FM_ERR_INVALID_ARG;
+  if (out_dtype != FM_F32 && out_dtype != FM_F16) return FM_ERR_INVALID_ARG;
+  fm_status st = fm::check_filter_args(sr, n_fft, n_mels, f_min, &f_max, mel_scale, norm);
+  if (st != FM_OK) return st;
+  if (!fm::is_supported_nfft(n_fft) || n_mels > 256 || (hop % 2) != 0) return FM_ERR_UNSUPPORTED;
+  const fm::Variant* var = fm::find_variant(n_fft);
+  if (var == nullptr) return FM_ERR_UNSUPPORTED;
+
+  // host tables (double precision, rounded to float)
+  std::vector<int> ms, ml, mo;
+  std::vector<float> mw, win;
+  std::vector<float2> twh, twf;
+  try {
+    fm::build_filterbank(sr, n_fft, n_mels, f_min, f_max, mel_scale == FM_MEL_SLANEY, norm == FM_NORM_SLANEY, ms,
+                         ml, mo, mw);
+    fm::build_window(n_fft, win_length, win);
+    fm::build_twiddles(n_fft / 2, n_fft / 2, twh);
+    fm::build_twiddles(n_fft, n_fft / 2 + 1, twf);
+  } catch (const std::bad_alloc&) {
+    return FM_ERR_OOM;
+  }
+  const int nnz = (int)mw.size();
+
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FM_ERR_CUDA;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
+  const fm::SmemLayout lay = fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile);
+  if (lay.total > (size_t)prop.sharedMemPerBlockOptin) return FM_ERR_UNSUPPORTED;
+  // allow the device maximum once, so plans of different sizes never undercut each other
+  if (cudaFuncSetAttribute(var->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)prop.sharedMemPerBlockOptin) != cudaSuccess)
+    return FM_ERR_CUDA;
+  int bps = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, var->fn, var->threads, lay.total) != cudaSuccess)
+    return FM_ERR_CUDA;
+  if (bps <= 0) return FM_ERR_UNSUPPORTED;
+
+  fm_plan* p = new (std::nothrow) fm_plan();
+  if (p == nullptr) return FM_ERR_OOM;
+  p->device = dev;
+  p->sr = sr;
+  p->n_fft = n_fft;
+  p->hop = hop;
+  p->win_length = win_length;
+  p->n_mels = n_mels;
+  p->f_min = f_min;
+  p->f_max = f_max;
+  p->power = power;
+  p->mel_scale = mel_scale;
+  p->norm = norm;
+  p->in_dtype = in_dtype;
+  p->out_dtype = out_dtype;
+  p->power_mode = power == 2.0 ? 0 : power == 1.0 ? 1 : 2;
+  p->var = var;
+  p->nnz = nnz;
+  p->smem = lay.total;
+  p->blocks_per_sm = bps;
+  p->num_sms = prop.multiProcessorCount;
+  p->grid_limit = bps * prop.multiProcessorCount;
+
+  // one device blob: window | tw_half | tw_full | start | len | off | weights | err
+  const int M = n_fft / 2;
+  size_t o = 0;
+  const size_t o_win = o;  o = fm::align16(o + sizeof(float) * n_fft);
+  const size_t o_twh = o;  o = fm::align16(o + sizeof(float2) * M);
+  const size_t o_twf = o;  o = fm::align16(o + sizeof(float2) * (M + 1));
+  const size_t o_ms = o;   o = fm::align16(o + sizeof(int) * n_mels);
+  const size_t o_ml = o;   o = fm::align16(o + sizeof(int) * n_mels);
+  const size_t o_mo = o;   o = fm::align16(o + sizeof(int) * (n_mels + 1));
+  const size_t o_mw = o;   o = fm::align16(o + sizeof(float) * (nnz > 0 ? nnz : 1));
+  const size_t o_err = o;  o = fm::align16(o + sizeof(unsigned) * 4);
+  std::vector<unsigned char> blob(o, 0);
+  std::memcpy(blob.data() + o_win, win.data(), sizeof(float) * n_fft);
+  std::memcpy(blob.data() + o_twh, twh.data(), sizeof(float2) * M);
+  std::memcpy(blob.data() + o_twf, twf.data(), sizeof(float2) * (M + 1));
+  std::memcpy(blob.data() + o_ms, ms.data(), sizeof(int) * n_mels);
+  std::memcpy(blob.data() + o_ml, ml.data(), sizeof(int) * n_mels);
+  std::memcpy(blob.data() + o_mo, mo.data(), sizeof(int) * (n_mels + 1));
+  if (nnz > 0) std::memcpy(blob.data() + o_mw, mw.data(), sizeof(float) * nnz);
+
+  cudaError_t e = cudaMalloc(&p->dmem, o);
+  if (e != cudaSuccess) {
+    delete p;
+    return from_cuda(e);
+  }
+  e = cudaMemcpy(p->dmem, blob.data(), o, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(p->dmem);
+    delete p;
+    return from_cuda(e);
+  }
+  unsigned char* base = static_cast<unsigned char*>(p->dmem);
+  p->window = reinterpret_cast<float*>(base + o_win);
+  p->tw_half = reinterpret_cast<float2*>(base + o_twh);
+  p->tw_full = reinterpret_cast<float2*>(base + o_twf);
+  p->mel_start = reinterpret_cast<int*>(base + o_ms);
+  p->mel_len = reinterpret_cast<int*>(base + o_ml);
+  p->mel_off = reinterpret_cast<int*>(base + o_mo);
+  p->mel_w = reinterpret_cast<float*>(base + o_mw);
+  p->err = reinterpret_cast<unsigned*>(base + o_err);
+  *out = p;
+  return FM_OK;
+}
+
+extern "C" fm_status fm_plan_destroy(fm_plan* plan) {
+  if (plan == nullptr) return FM_OK;
+  cudaError_t e = cudaSuccess;
+  if (plan->dmem) e = cudaFree(plan->dmem);
+  delete plan;
+  return e == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+extern "C" int64_t fm_n_frames(const fm_plan* plan, int64_t T) {
+  if (plan == nullptr || T < 0) return -1;
+  return 1 + T / plan->hop;
+}
+
+static fm_status check_forward(const fm_plan* plan, const void* in, int64_t B, int64_t T, const void* out) {
+  if (plan == nullptr || B < 0) return FM_ERR_INVALID_ARG;
+  if (B == 0) return FM_OK;
+  if (in == nullptr || out == nullptr) return FM_ERR_INVALID_ARG;
+  if (T <= plan->n_fft / 2) return FM_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t)1 << 62;
+  if (T > lim / B) return FM_ERR_INVALID_ARG;
+  const int64_t nf = 1 + T / plan->hop;
+  if (nf > INT_MAX) return FM_ERR_INVALID_ARG;
+  if (nf * plan->n_mels > lim / B) return FM_ERR_INVALID_ARG;
+  return FM_OK;
+}
+
+extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64_t B, int64_t T, void* d_out,
+                                    fm_stream_t stream) {
+  fm_status st = check_forward(plan, d_in, B, T, d_out);
+  if (st != FM_OK || B == 0) return st;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device) return FM_ERR_CUDA;
+
+  const fm::Variant* v = plan->var;
+  fm::KernelParams prm;
+  prm.in = d_in;
+  prm.out = d_out;
+  prm.B = B;
+  prm.T = T;
+  prm.n_frames = (int)(1 + T / plan->hop);
+  prm.hop = plan->hop;
+  prm.pad = plan->n_fft / 2;
+  prm.in_dtype = plan->in_dtype;
+  prm.out_dtype = plan->out_dtype;
+  prm.n_mels = plan->n_mels;
+  prm.nnz = plan->nnz;
+  prm.power_mode = plan->power_mode;
+  prm.power = (float)plan->power;
+  prm.tiles_per_signal = (prm.n_frames + v->frames_per_tile - 1) / v->frames_per_tile;
+  prm.total_tiles = (long long)B * prm.tiles_per_signal;
+  prm.window = plan->window;
+  prm.tw_half = plan->tw_half;
+  prm.tw_full = plan->tw_full;
+  prm.mel_start = plan->mel_start;
+  prm.mel_len = plan->mel_len;
+  prm.mel_off = plan->mel_off;
+  prm.mel_w = plan->mel_w;
+  prm.err = plan->err;
+
+  const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
+  void* args[] = {&prm};
+  cudaError_t e = cudaLaunchKernel(v->fn, dim3((unsigned)grid), dim3(v->threads), args, plan->smem,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+extern "C" fm_status fm_mel_forward_host(const fm_plan* plan, const void* h_in, int64_t B, int64_t T,
+                                         void* h_out, void* d_in_scratch, void* d_out_scratch,
+                                         fm_stream_t stream) {
+  fm_status st = check_forward(plan, h_in, B, T, h_out);
+  if (st != FM_OK || B == 0) return st;
+  if (d_in_scratch == nullptr || d_out_scratch == nullptr) return FM_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t in_bytes = (size_t)B * (size_t)T * dtype_size(plan->in_dtype);
+  const size_t out_bytes = (size_t)B * plan->n_mels * (size_t)(1 + T / plan->hop) * dtype_size(plan->out_dtype);
+  if (cudaMemcpyAsync(d_in_scratch, h_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return FM_ERR_CUDA;
+  st = fm_mel_forward(plan, d_in_scratch, B, T, d_out_scratch, stream);
+  if (st != FM_OK) return st;
+  if (cudaMemcpyAsync(h_out, d_out_scratch, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FM_ERR_CUDA;
+  return FM_OK;
+}
+
+extern "C" fm_status fm_plan_get_info(const fm_plan* plan, fm_plan_info* info) {
+  if (plan == nullptr || info == nullptr) return FM_ERR_INVALID_ARG;
+  info->n_fft = plan->n_fft;
+  info->hop = plan->hop;
+  info->win_length = plan->win_length;
+  info->n_mels = plan->n_mels;
+  info->n_freqs = plan->n_fft / 2 + 1;
+  info->in_dtype = plan->in_dtype;
+  info->out_dtype = plan->out_dtype;
+  info->nnz = plan->nnz;
+  info->frames_per_tile = plan->var->frames_per_tile;
+  info->threads_per_block = plan->var->threads;
+  info->blocks_per_sm = plan->blocks_per_sm;
+  info->grid_limit = plan->grid_limit;
+  info->smem_bytes = (int)plan->smem;
+  info->device = plan->device;
+  return FM_OK;
+}
+
+extern "C" fm_status fm_plan_poll_error(const fm_plan* plan) {
+  if (plan == nullptr) return FM_ERR_INVALID_ARG;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, plan->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FM_ERR_CUDA;
+  if (word == 0) return FM_OK;
+  const unsigned zero = 0;
+  if (cudaMemcpy(plan->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FM_ERR_CUDA;
+  return word <= FM_ERR_KERNEL_TIMEOUT ? (fm_status)word : FM_ERR_KERNEL_TIMEOUT;
+}
+
+extern "C" const char* fm_status_string(fm_status status) {
+  switch (status) {
+    case FM_OK: return "FM_OK";
+    case FM_ERR_INVALID_ARG: return "FM_ERR_INVALID_ARG";
+    case FM_ERR_UNSUPPORTED: return "FM_ERR_UNSUPPORTED";
+    case FM_ERR_CUDA: return "FM_ERR_CUDA";
+    case FM_ERR_OOM: return "FM_ERR_OOM";
+    case FM_ERR_KERNEL_TIMEOUT: return "FM_ERR_KERNEL_TIMEOUT";
+  }
+  return "FM_ERR_UNKNOWN";
+}

@@ -1,0 +1,127 @@
+"""Host-only tests of the C ABI: no kernel runs here (no GPU needed)."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle.mel_oracle as o
+from mel_spectrogram_gb300 import _binding as fb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fm_mel.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mel_spectrogram_gb300.build import build
+
+    build()
+    return fb.lib()
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fm_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_what_the_binding_exports():
+    assert declared_functions() == sorted(fb.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    assert fb.status_string(fb.FM_OK) == "FM_OK"
+    assert fb.status_string(fb.FM_ERR_KERNEL_TIMEOUT) == "FM_ERR_KERNEL_TIMEOUT"
+    assert fb.status_string(99) == "FM_ERR_UNKNOWN"
+
+
+CSR_CASES = [
+    (16000, 400, 80, 0.0, 8000.0, "htk", None),
+    (16000, 400, 128, 0.0, 8000.0, "htk", None),
+    (16000, 1024, 80, 0.0, 8000.0, "htk", None),
+    (22050, 2048, 128, 0.0, 11025.0, "slaney", "slaney"),
+    (16000, 512, 40, 125.0, 7600.0, "slaney", None),
+    (44100, 256, 256, 30.0, 0.0, "htk", "slaney"),
+    (8000, 64, 1, 0.0, 4000.0, "htk", None),
+]
+
+
+@pytest.mark.parametrize("case", CSR_CASES)
+def test_host_filterbank_matches_oracle(L, case):
+    sr, n_fft, n_mels, f_min, f_max, scale, norm = case
+    start, ln, off, w = fb.fm_mel_filterbank_csr(sr, n_fft, n_mels, f_min, f_max, scale, norm)
+    F = o.mel_filterbank(n_fft, sr, n_mels, f_min, f_max if f_max > 0 else sr / 2, scale, norm)
+    dense = np.zeros_like(F)
+    assert off[0] == 0 and off[-1] == len(w)
+    for m in range(n_mels):
+        assert off[m + 1] - off[m] == ln[m]
+        dense[m, start[m] : start[m] + ln[m]] = w[off[m] : off[m + 1]]
+    tol = 1e-6 * F.max()
+    assert np.abs(dense - F).max() <= tol
+    # support: every oracle weight above rounding level is inside the stored run
+    big = F > 1e-9 * F.max()
+    assert np.all(dense[big] > 0)
+
+
+def test_empty_filters_have_zero_length(L):
+    # HTK, 128 mels over 201 bins at 40 Hz spacing: the lowest filters are
+    # narrower than a bin and some contain none.
+    start, ln, off, w = fb.fm_mel_filterbank_csr(16000, 400, 128, 0.0, 8000.0, "htk", None)
+    F = o.mel_filterbank(400, 16000, 128, 0.0, 8000.0, "htk", None)
+    empty = np.nonzero(F.max(axis=1) == 0)[0]
+    assert empty.size > 0
+    assert np.all(ln[empty] == 0)
+
+
+@pytest.mark.parametrize(
+    "kw",
+    [
+        dict(sr=0), dict(n_fft=0), dict(hop=0), dict(n_mels=0), dict(win_length=500), dict(f_min=-1.0),
+        dict(f_max=9000.0), dict(f_min=5000.0, f_max=4000.0), dict(power=0.0), dict(power=float("nan")),
+        dict(out_dtype=1), dict(in_dtype=7), dict(mel_scale=5), dict(norm=3),
+    ],
+)
+def test_plan_create_rejects_invalid(L, kw):
+    args = dict(sr=16000, n_fft=400, hop=160, win_length=400, n_mels=80, f_min=0.0, f_max=8000.0, power=2.0,
+                mel_scale=0, norm=0, in_dtype=0, out_dtype=0)
+    args.update(kw)
+    h = C.c_void_p(1234)
+    st = L.fm_plan_create(C.byref(h), *args.values())
+    assert st == fb.FM_ERR_INVALID_ARG
+    assert h.value is None
+
+
+@pytest.mark.parametrize("kw", [dict(n_fft=300), dict(n_fft=4096), dict(n_mels=257), dict(hop=161)])
+def test_plan_create_reports_unsupported(L, kw):
+    args = dict(sr=16000, n_fft=400, hop=160, win_length=0, n_mels=80, f_min=0.0, f_max=0.0, power=2.0,
+                mel_scale=0, norm=0, in_dtype=0, out_dtype=0)
+    args.update(kw)
+    h = C.c_void_p()
+    assert L.fm_plan_create(C.byref(h), *args.values()) == fb.FM_ERR_UNSUPPORTED
+
+
+def test_null_arguments(L):
+    assert L.fm_plan_create(None, 16000, 400, 160, 400, 80, 0.0, 0.0, 2.0, 0, 0, 0, 0) == fb.FM_ERR_INVALID_ARG
+    assert L.fm_mel_forward(None, None, 1, 1000, None, None) == fb.FM_ERR_INVALID_ARG
+    assert L.fm_plan_destroy(None) == fb.FM_OK
+    assert L.fm_n_frames(None, 100) == -1
+    assert L.fm_plan_get_info(None, None) == fb.FM_ERR_INVALID_ARG
+    assert L.fm_plan_poll_error(None) == fb.FM_ERR_INVALID_ARG
+    nnz = C.c_int64(0)
+    assert L.fm_mel_filterbank_csr(16000, 400, 80, 0.0, 0.0, 0, 0, None, None, None, None, None) == \
+        fb.FM_ERR_INVALID_ARG
+    # too small a weights buffer is refused
+    buf = (C.c_float * 3)()
+    nnz = C.c_int64(3)
+    assert L.fm_mel_filterbank_csr(16000, 400, 80, 0.0, 0.0, 0, 0, None, None, None, buf, C.byref(nnz)) == \
+        fb.FM_ERR_INVALID_ARG
+    assert nnz.value > 3
