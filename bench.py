@@ -1,0 +1,405 @@
+"""Benchmark of the fused mel-spectrogram kernel on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole path (pad, frame, window, real DFT, |X|^p,
+mel projection) over one batch of the workload: one fm_mel_forward launch.
+Steps rotate over 16 input/output buffer sets (more bytes than the 129 MB
+L2), are captured in a CUDA graph and replayed; the timed region is exactly K
+steps between barriers and device synchronisations, timed with CUDA events on
+the launching stream. Under torchrun every rank runs its own replica (weak
+scaling, no collective on the data path); the reported time is the max over
+ranks. `--impl reference` times the float64 CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mel_spectrogram_gb300.workloads import WORKLOADS, make_input  # noqa: E402
+
+METRIC = "mel frames/sec and achieved HBM GB/s (fraction of roofline) at B=8×480000 fp32"
+BUFFER_SETS = 16
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["fm_kernel.cuh", "fm_internal.h", "fm_kernel_n400.cu", "fm_kernel_n1024.cu", "fm_kernel_n2048.cu"]
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "mel_spectrogram_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_sha") != kernel_sha():
+        return None  # the kernel changed since the counters were taken
+    v = d.get("bytes_per_launch", {}).get(workload)
+    return float(v) if v is not None else None
+
+
+def describe(w) -> str:
+    norm = "Slaney norm" if w.norm else "no norm"
+    return (f"{w.name}: B={w.B} x T={w.T} {w.in_dtype}, sr {w.sr}, n_fft {w.n_fft}, hop {w.hop}, "
+            f"{w.n_mels} mels {w.mel_scale.upper()} {norm}, power {w.power:g}, {w.out_dtype} out "
+            f"-> [{w.B},{w.n_mels},{w.n_frames}]")
+
+
+def conventional_flops(w) -> float:
+    """Per frame: real FFT 2.5 N log2 N + window N + power 3 n_freqs + mel 2 nnz."""
+    from mel_spectrogram_gb300 import fm_mel_filterbank_csr
+
+    _, _, _, wts = fm_mel_filterbank_csr(w.sr, w.n_fft, w.n_mels, w.f_min, w.f_max, w.mel_scale, w.norm)
+    N = w.n_fft
+    per_frame = 2.5 * N * np.log2(N) + N + 3 * (N // 2 + 1) + 2 * len(wts)
+    return per_frame * w.B * w.n_frames
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self, t_start: float, t_end: float) -> dict:
+        import datetime
+
+        rows = [r.split(",") for r in (self.out or "").strip().splitlines() if r.count(",") >= 7]
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if ts < t_start - 0.05 or ts > t_end + 0.05:
+                    continue  # outside the timed region
+                mhz.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for name, flag in zip(names, r[4:8]):
+                if flag.strip().lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------- GPU arm
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return world, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def run_gpu_arm(args) -> dict | None:
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from mel_spectrogram_gb300.build import build
+
+    if local == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    from mel_spectrogram_gb300 import _binding as fb
+
+    w = WORKLOADS[args.workload]
+    x = make_input(w)
+    tdt = {"f32": torch.float32, "i16": torch.int16, "f16": torch.float16}
+    plan = fb.fm_plan_create(w.sr, w.n_fft, w.hop, w.win_length, w.n_mels, w.f_min, w.f_max, w.power,
+                             w.mel_scale, w.norm, w.in_dtype, w.out_dtype)
+    info = fb.fm_plan_get_info(plan)
+    nf = fb.fm_n_frames(plan, w.T)
+    xin = torch.from_numpy(x).cuda()
+    d_in = [xin.clone() for _ in range(BUFFER_SETS)]
+    d_out = [torch.empty((w.B, w.n_mels, nf), dtype=tdt[w.out_dtype], device="cuda") for _ in range(BUFFER_SETS)]
+    s = torch.cuda.Stream()
+
+    def launch(i):
+        fb.fm_mel_forward(plan, d_in[i].data_ptr(), w.B, w.T, d_out[i].data_ptr(), s.cuda_stream)
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(s):
+        for i in range(W):
+            launch(i % BUFFER_SETS)
+    s.synchronize()
+    graphs = {}
+    for n in sorted({BUFFER_SETS, K % BUFFER_SETS} - {0}):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                launch(i)
+        graphs[n] = g
+    with torch.cuda.stream(s):  # upload and warm the graphs
+        for g in graphs.values():
+            g.replay()
+    s.synchronize()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start = time.time()
+        with torch.cuda.stream(s):
+            ev0.record(s)
+            for _ in range(K // BUFFER_SETS):
+                graphs[BUFFER_SETS].replay()
+            if K % BUFFER_SETS:
+                graphs[K % BUFFER_SETS].replay()
+            ev1.record(s)
+        s.synchronize()
+        torch.cuda.synchronize()
+        t_end = time.time()
+        if world > 1:
+            dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary(t_start, t_end)
+    assert fb.fm_plan_poll_error(plan) == fb.FM_OK
+
+    # end to end through the public C ABI with host buffers (copies in the region)
+    Ke = max(3, min(K, args.e2e_steps))
+    h_in = torch.from_numpy(x).pin_memory()
+    h_out = torch.empty((w.B, w.n_mels, nf), dtype=tdt[w.out_dtype]).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step(i):
+        fb.fm_mel_forward_host(plan, h_in.data_ptr(), w.B, w.T, h_out.data_ptr(), d_in[i].data_ptr(),
+                               d_out[i].data_ptr(), s.cuda_stream)
+
+    for i in range(3):
+        e2e_step(i)
+    s.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0.record(s)
+    for i in range(Ke):
+        e2e_step(i % BUFFER_SETS)
+    e1.record(s)
+    s.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    fb.fm_plan_destroy(plan)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    frames_step = w.B * nf
+    step_s = ms / 1e3 / K
+    pk = peaks()
+    in_b, out_b = w.in_bytes(), w.out_bytes()
+    achieved = (in_b + out_b) / step_s / 1e9
+    flops = conventional_flops(w)
+    props = torch.cuda.get_device_properties(0)
+    clk_mhz = clocks["sm_mhz"] or pk["sm_max_mhz"]
+    fp32_peak = props.multi_processor_count * 128 * 2 * clk_mhz * 1e6 / 1e12
+    line = {
+        "metric": METRIC,
+        "value": world * frames_step / step_s,
+        "unit": "frames/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": f"synthetic, seeded ({w.recipe}, seed {w.seed})",
+        "config": {
+            "workload": describe(w),
+            "B": w.B, "T": w.T, "n_fft": w.n_fft, "hop": w.hop, "n_mels": w.n_mels,
+            "in_dtype": w.in_dtype, "out_dtype": w.out_dtype,
+            "l2": f"{BUFFER_SETS} rotating input/output sets, "
+                  f"{BUFFER_SETS * (in_b + out_b) / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2",
+            "launch": f"CUDA graph of {BUFFER_SETS} fm_mel_forward launches, replayed",
+            "grid": min(info["grid_limit"], w.B * -(-nf // info["frames_per_tile"])),
+            "block": info["threads_per_block"], "smem_bytes": info["smem_bytes"],
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "audio_seconds_per_s": world * w.B * w.T / w.sr / step_s,
+        "hbm_gbs": achieved,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": pk["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"],
+            "peak_source": f"{pk['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+            "algorithmic_bytes_per_launch": in_b + out_b,
+            "traffic": recorded_traffic(w.name),
+        },
+        "fp32": {"achieved_tflops": flops / step_s / 1e12, "peak_tflops": fp32_peak,
+                 "frac": flops / step_s / 1e12 / fp32_peak,
+                 "peak_basis": f"{props.multi_processor_count} SMs x 128 lanes x 2 x {clk_mhz:.0f} MHz"},
+        "e2e": {"value": world * frames_step * Ke / (e_ms / 1e3), "unit": "frames/s",
+                "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b, "steps": Ke,
+                "api": "fm_mel_forward_host (pinned host buffers, copies + kernel per step)"},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(w, x, args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------- oracle on the host
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_segment(w, x, frames: int):
+    """Signal 0 cut so that centre framing yields about `frames` frames."""
+    Ts = max(w.n_fft // 2 + 1, (frames - 1) * w.hop)
+    Ts = min(Ts, w.T)
+    return x[0:1, :Ts], 1 + Ts // w.hop
+
+
+def oracle_run(w, seg):
+    import oracle.mel_oracle as o
+
+    return o.mel_spectrogram(seg, w.sr, w.n_fft, w.hop, w.n_mels, w.f_min, w.f_max, w.power, w.mel_scale, w.norm,
+                             w.win_length)
+
+
+def oracle_baseline(w, x, seconds: float) -> dict:
+    """The oracle as it stands, timed on a bounded sample (repeated for ~seconds)."""
+    seg, fr = oracle_segment(w, x, min(w.n_frames, 512))
+    oracle_run(w, seg)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_run(w, seg)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": n * fr / el, "unit": "frames/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"{fr} frames of signal 0 (first {seg.shape[1]} samples), {n} repeats in {el:.1f} s; "
+                      f"float64 numpy, naive DFT as a matmul; BLAS threads = host cores"}
+
+
+def run_reference_arm(args) -> dict | None:
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    x = make_input(w)
+    probe, fr_probe = oracle_segment(w, x, 64)
+    oracle_run(w, probe)
+    t0 = time.perf_counter()
+    oracle_run(w, probe)
+    per_frame = (time.perf_counter() - t0) / fr_probe
+    K, W = args.steps, args.warmup
+    budget = args.ref_seconds
+    frames = int(max(1, min(w.n_frames, budget / max(1, K + W) / per_frame)))
+    seg, fr = oracle_segment(w, x, frames)
+    for _ in range(W):
+        oracle_run(w, seg)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_run(w, seg)
+    el = time.perf_counter() - t0
+    v = fr * K / el
+    sample = f"{fr} frames of signal 0 per step (first {seg.shape[1]} samples), {K} steps in {el:.1f} s"
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "frames/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": el * 1e3 / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": f"synthetic, seeded ({w.recipe}, seed {w.seed})",
+        "config": {"workload": describe(w), "B": w.B, "T": w.T, "n_fft": w.n_fft, "hop": w.hop,
+                   "n_mels": w.n_mels, "in_dtype": w.in_dtype, "out_dtype": w.out_dtype,
+                   "parallelism": "host cores (rank 0 only)"},
+        "cpu_baseline": {"value": v, "unit": "frames/s", "cores": host_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="speech", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference_arm(args) if args.impl == "reference" else run_gpu_arm(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

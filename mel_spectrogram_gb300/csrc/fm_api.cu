@@ -36,12 +36,10 @@ struct fm_plan {
   size_t smem;
   int blocks_per_sm, grid_limit, num_sms;
   void* dmem;
-  float* window;
+  float4* p1;
   float2* tw_half;
   float2* tw_full;
-  int* mel_start;
-  int* mel_len;
-  int* mel_off;
+  int4* mel;
   float* mel_w;
   unsigned* err;
 };
@@ -94,7 +92,8 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   cudaDeviceProp prop;
   if (cudaGetDevice(&dev) != cudaSuccess) return FM_ERR_CUDA;
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
-  const fm::SmemLayout lay = fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile);
+  const fm::SmemLayout lay = fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile,
+                                             in_dtype == FM_F32 ? 4 : 2, var->in_buffers);
   if (lay.total > (size_t)prop.sharedMemPerBlockOptin) return FM_ERR_UNSUPPORTED;
   // allow the device maximum once, so plans of different sizes never undercut each other
   if (cudaFuncSetAttribute(var->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -128,24 +127,39 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   p->num_sms = prop.multiProcessorCount;
   p->grid_limit = bps * prop.multiProcessorCount;
 
-  // one device blob: window | tw_half | tw_full | start | len | off | weights | err
+  // pass-1 table: role p, step q -> window at 2n, 2n+1 (n = p + P q) and the
+  // tile offset of sample 2n (rows of hop samples, stride in_row_stride)
   const int M = n_fft / 2;
+  const int S = fm::in_row_stride(hop);
+  const float in_scale = in_dtype == FM_I16 ? 1.0f / 32768.0f : 1.0f;  // exact power of two
+  std::vector<float4> p1(M);
+  for (int pp = 0; pp < var->P; ++pp)
+    for (int q = 0; q < var->Q; ++q) {
+      const int j = 2 * (pp + var->P * q);
+      const int off = (j / hop) * S + (j % hop);
+      float4 e;
+      e.x = win[j] * in_scale;
+      e.y = win[j + 1] * in_scale;
+      std::memcpy(&e.z, &off, sizeof(int));
+      e.w = 0.0f;
+      p1[pp * var->Q + q] = e;
+    }
+  std::vector<int4> mel(n_mels);
+  for (int m = 0; m < n_mels; ++m) mel[m] = make_int4(ms[m], ml[m], mo[m], 0);
+
+  // one device blob: p1 | tw_half | tw_full | mel | weights | err
   size_t o = 0;
-  const size_t o_win = o;  o = fm::align16(o + sizeof(float) * n_fft);
+  const size_t o_p1 = o;   o = fm::align16(o + sizeof(float4) * M);
   const size_t o_twh = o;  o = fm::align16(o + sizeof(float2) * M);
   const size_t o_twf = o;  o = fm::align16(o + sizeof(float2) * (M + 1));
-  const size_t o_ms = o;   o = fm::align16(o + sizeof(int) * n_mels);
-  const size_t o_ml = o;   o = fm::align16(o + sizeof(int) * n_mels);
-  const size_t o_mo = o;   o = fm::align16(o + sizeof(int) * (n_mels + 1));
+  const size_t o_mel = o;  o = fm::align16(o + sizeof(int4) * n_mels);
   const size_t o_mw = o;   o = fm::align16(o + sizeof(float) * (nnz > 0 ? nnz : 1));
   const size_t o_err = o;  o = fm::align16(o + sizeof(unsigned) * 4);
   std::vector<unsigned char> blob(o, 0);
-  std::memcpy(blob.data() + o_win, win.data(), sizeof(float) * n_fft);
+  std::memcpy(blob.data() + o_p1, p1.data(), sizeof(float4) * M);
   std::memcpy(blob.data() + o_twh, twh.data(), sizeof(float2) * M);
   std::memcpy(blob.data() + o_twf, twf.data(), sizeof(float2) * (M + 1));
-  std::memcpy(blob.data() + o_ms, ms.data(), sizeof(int) * n_mels);
-  std::memcpy(blob.data() + o_ml, ml.data(), sizeof(int) * n_mels);
-  std::memcpy(blob.data() + o_mo, mo.data(), sizeof(int) * (n_mels + 1));
+  std::memcpy(blob.data() + o_mel, mel.data(), sizeof(int4) * n_mels);
   if (nnz > 0) std::memcpy(blob.data() + o_mw, mw.data(), sizeof(float) * nnz);
 
   cudaError_t e = cudaMalloc(&p->dmem, o);
@@ -160,12 +174,10 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
     return from_cuda(e);
   }
   unsigned char* base = static_cast<unsigned char*>(p->dmem);
-  p->window = reinterpret_cast<float*>(base + o_win);
+  p->p1 = reinterpret_cast<float4*>(base + o_p1);
   p->tw_half = reinterpret_cast<float2*>(base + o_twh);
   p->tw_full = reinterpret_cast<float2*>(base + o_twf);
-  p->mel_start = reinterpret_cast<int*>(base + o_ms);
-  p->mel_len = reinterpret_cast<int*>(base + o_ml);
-  p->mel_off = reinterpret_cast<int*>(base + o_mo);
+  p->mel = reinterpret_cast<int4*>(base + o_mel);
   p->mel_w = reinterpret_cast<float*>(base + o_mw);
   p->err = reinterpret_cast<unsigned*>(base + o_err);
   *out = p;
@@ -222,12 +234,10 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.power = (float)plan->power;
   prm.tiles_per_signal = (prm.n_frames + v->frames_per_tile - 1) / v->frames_per_tile;
   prm.total_tiles = (long long)B * prm.tiles_per_signal;
-  prm.window = plan->window;
+  prm.p1 = plan->p1;
   prm.tw_half = plan->tw_half;
   prm.tw_full = plan->tw_full;
-  prm.mel_start = plan->mel_start;
-  prm.mel_len = plan->mel_len;
-  prm.mel_off = plan->mel_off;
+  prm.mel = plan->mel;
   prm.mel_w = plan->mel_w;
   prm.err = plan->err;
 

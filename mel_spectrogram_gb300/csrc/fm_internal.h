@@ -24,19 +24,22 @@ struct KernelParams {
   float power;
   int tiles_per_signal;
   long long total_tiles;
-  const float* window;    // n_fft, periodic Hann * 1/2 (the 1/2 of the real-FFT split)
+  // pass-1 table, one float4 per (role p, q) at [p * Q + q]: the window at
+  // samples 2n and 2n+1 (n = p + P q, times 1/2 for the real-FFT split and
+  // times 2^-15 for int16 input) and, as int bits, the offset of sample 2n in
+  // the staged tile relative to the frame's first row.
+  const float4* p1;
   const float2* tw_half;  // W_{n_fft/2}^j, j < n_fft/2, stored (cos, -sin)
   const float2* tw_full;  // W_{n_fft}^k, k <= n_fft/2, stored (cos, -sin)
-  const int* mel_start;   // n_mels
-  const int* mel_len;     // n_mels
-  const int* mel_off;     // n_mels (+1)
+  const int4* mel;        // n_mels x {start, len, offset, 0}
   const float* mel_w;     // nnz
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
 };
 
-// Row stride (floats) of the staged input tile: rows hold `hop` samples; a
-// stride of 2 (mod 4) floats makes the per-frame float2 reads of a half-warp
-// fall on 16 distinct bank pairs.
+// Row stride (elements) of the staged input tile: rows hold `hop` samples; a
+// stride of 2 (mod 4) elements makes the per-frame sample-pair reads of the
+// lanes of a warp fall on distinct banks (float2 for f32, one word for
+// 16-bit samples).
 __host__ __device__ inline int in_row_stride(int hop) { return hop + ((hop % 4 == 0) ? 2 : 0); }
 __host__ __device__ inline int in_rows(int n_fft, int hop, int frames_per_tile) {
   return frames_per_tile + (n_fft - 1) / hop;
@@ -46,22 +49,21 @@ __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(
 
 // Dynamic shared-memory layout of one CTA, in bytes from the base.
 struct SmemLayout {
-  size_t window, tw_half, tw_full, mel_start, mel_len, mel_off, mel_w, in_tile, xbuf, total;
+  size_t p1, tw_half, tw_full, mel, mel_w, in_tile, in_tile_bytes, xbuf, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int n_fft, int hop, int n_mels, int nnz,
-                                                  int frames_per_tile) {
+__host__ __device__ inline SmemLayout smem_layout(int n_fft, int hop, int n_mels, int nnz, int frames_per_tile,
+                                                  int in_esize, int n_in_buffers) {
   const int M = n_fft / 2;
   SmemLayout L;
   size_t o = 0;
-  L.window = o;    o = align16(o + sizeof(float) * n_fft);
+  L.p1 = o;        o = align16(o + sizeof(float4) * M);
   L.tw_half = o;   o = align16(o + sizeof(float2) * M);
   L.tw_full = o;   o = align16(o + sizeof(float2) * (M + 1));
-  L.mel_start = o; o = align16(o + sizeof(int) * n_mels);
-  L.mel_len = o;   o = align16(o + sizeof(int) * n_mels);
-  L.mel_off = o;   o = align16(o + sizeof(int) * n_mels);
+  L.mel = o;       o = align16(o + sizeof(int4) * n_mels);
   L.mel_w = o;     o = align16(o + sizeof(float) * (nnz > 0 ? nnz : 1));
-  L.in_tile = o;   o = align16(o + sizeof(float) * (size_t)in_rows(n_fft, hop, frames_per_tile) * in_row_stride(hop));
+  L.in_tile_bytes = align16((size_t)in_esize * in_rows(n_fft, hop, frames_per_tile) * in_row_stride(hop));
+  L.in_tile = o;   o += L.in_tile_bytes * n_in_buffers;
   L.xbuf = o;      o = align16(o + sizeof(float2) * (size_t)frames_per_tile * (M + 1));
   L.total = o;
   return L;
@@ -73,6 +75,7 @@ struct Variant {
   int P, Q;             // pass 1: P roles x Q-point DFTs; pass 2: Q x P-point DFTs
   int frames_per_tile;  // G: frames per tile = lanes per role
   int threads;          // P * G
+  int in_buffers;       // 2: the next tile's input lands while this one computes
   const void* fn;       // __global__ void(KernelParams)
 };
 
