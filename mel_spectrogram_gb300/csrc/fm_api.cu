@@ -41,7 +41,11 @@ struct fm_plan {
   float2* tw_full;
   int4* mel;
   float* mel_w;
+  float4* tw_half4;
+  float4* tw_full4;
+  float2* mel_w2;
   unsigned* err;
+  fm::X2Tables* x2;  // device tables of the two-frames-per-thread kernel (inside dmem)
 };
 
 namespace {
@@ -92,20 +96,25 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   cudaDeviceProp prop;
   if (cudaGetDevice(&dev) != cudaSuccess) return FM_ERR_CUDA;
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
-  const fm::SmemLayout lay = fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile,
-                                             in_dtype == FM_F32 ? 4 : 2, var->in_buffers);
-  if (lay.total > (size_t)prop.sharedMemPerBlockOptin) return FM_ERR_UNSUPPORTED;
+  const int in_esize = in_dtype == FM_F32 ? 4 : 2;
+  const size_t smem_total =
+      var->kind == 1 ? fm::smem_layout_x2(n_fft, hop, n_mels, nnz, in_esize).total
+                     : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
+  if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || n_mels > fm::kX2MaxMels || nnz > fm::kX2MaxNnz))
+    return FM_ERR_UNSUPPORTED;
+  if (smem_total > (size_t)prop.sharedMemPerBlockOptin) return FM_ERR_UNSUPPORTED;
   // allow the device maximum once, so plans of different sizes never undercut each other
   if (cudaFuncSetAttribute(var->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)prop.sharedMemPerBlockOptin) != cudaSuccess)
     return FM_ERR_CUDA;
   int bps = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, var->fn, var->threads, lay.total) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, var->fn, var->threads, smem_total) != cudaSuccess)
     return FM_ERR_CUDA;
   if (bps <= 0) return FM_ERR_UNSUPPORTED;
 
   fm_plan* p = new (std::nothrow) fm_plan();
   if (p == nullptr) return FM_ERR_OOM;
+  p->x2 = nullptr;
   p->device = dev;
   p->sr = sr;
   p->n_fft = n_fft;
@@ -122,7 +131,7 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   p->power_mode = power == 2.0 ? 0 : power == 1.0 ? 1 : 2;
   p->var = var;
   p->nnz = nnz;
-  p->smem = lay.total;
+  p->smem = smem_total;
   p->blocks_per_sm = bps;
   p->num_sms = prop.multiProcessorCount;
   p->grid_limit = bps * prop.multiProcessorCount;
@@ -146,6 +155,12 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
     }
   std::vector<int4> mel(n_mels);
   for (int m = 0; m < n_mels; ++m) mel[m] = make_int4(ms[m], ml[m], mo[m], 0);
+  // packed copies for the two-frames-per-thread kernel
+  std::vector<float4> twh4(M), twf4(M + 1);
+  for (int j = 0; j < M; ++j) twh4[j] = make_float4(twh[j].x, twh[j].x, twh[j].y, twh[j].y);
+  for (int j = 0; j <= M; ++j) twf4[j] = make_float4(twf[j].x, twf[j].x, twf[j].y, twf[j].y);
+  std::vector<float2> mw2(nnz > 0 ? nnz : 1);
+  for (int j = 0; j < nnz; ++j) mw2[j] = make_float2(mw[j], mw[j]);
 
   // one device blob: p1 | tw_half | tw_full | mel | weights | err
   size_t o = 0;
@@ -154,13 +169,28 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   const size_t o_twf = o;  o = fm::align16(o + sizeof(float2) * (M + 1));
   const size_t o_mel = o;  o = fm::align16(o + sizeof(int4) * n_mels);
   const size_t o_mw = o;   o = fm::align16(o + sizeof(float) * (nnz > 0 ? nnz : 1));
+  const size_t o_twh4 = o; o = fm::align16(o + sizeof(float4) * M);
+  const size_t o_twf4 = o; o = fm::align16(o + sizeof(float4) * (M + 1));
+  const size_t o_mw2 = o;  o = fm::align16(o + sizeof(float2) * mw2.size());
+  const size_t o_x2 = o;   o = fm::align16(o + (var->kind == 1 ? sizeof(fm::X2Tables) : 0));
   const size_t o_err = o;  o = fm::align16(o + sizeof(unsigned) * 4);
   std::vector<unsigned char> blob(o, 0);
+  if (var->kind == 1) {
+    fm::X2Tables* t = reinterpret_cast<fm::X2Tables*>(blob.data() + o_x2);
+    std::memcpy(t->p1, p1.data(), sizeof(float4) * M);
+    std::memcpy(t->tw_half, twh4.data(), sizeof(float4) * M);
+    std::memcpy(t->tw_full, twf4.data(), sizeof(float4) * (M + 1));
+    std::memcpy(t->mel, mel.data(), sizeof(int4) * n_mels);
+    if (nnz > 0) std::memcpy(t->mel_w, mw2.data(), sizeof(float2) * nnz);
+  }
   std::memcpy(blob.data() + o_p1, p1.data(), sizeof(float4) * M);
   std::memcpy(blob.data() + o_twh, twh.data(), sizeof(float2) * M);
   std::memcpy(blob.data() + o_twf, twf.data(), sizeof(float2) * (M + 1));
   std::memcpy(blob.data() + o_mel, mel.data(), sizeof(int4) * n_mels);
   if (nnz > 0) std::memcpy(blob.data() + o_mw, mw.data(), sizeof(float) * nnz);
+  std::memcpy(blob.data() + o_twh4, twh4.data(), sizeof(float4) * M);
+  std::memcpy(blob.data() + o_twf4, twf4.data(), sizeof(float4) * (M + 1));
+  std::memcpy(blob.data() + o_mw2, mw2.data(), sizeof(float2) * mw2.size());
 
   cudaError_t e = cudaMalloc(&p->dmem, o);
   if (e != cudaSuccess) {
@@ -179,7 +209,11 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   p->tw_full = reinterpret_cast<float2*>(base + o_twf);
   p->mel = reinterpret_cast<int4*>(base + o_mel);
   p->mel_w = reinterpret_cast<float*>(base + o_mw);
+  p->tw_half4 = reinterpret_cast<float4*>(base + o_twh4);
+  p->tw_full4 = reinterpret_cast<float4*>(base + o_twf4);
+  p->mel_w2 = reinterpret_cast<float2*>(base + o_mw2);
   p->err = reinterpret_cast<unsigned*>(base + o_err);
+  p->x2 = var->kind == 1 ? reinterpret_cast<fm::X2Tables*>(base + o_x2) : nullptr;
   *out = p;
   return FM_OK;
 }
@@ -239,12 +273,16 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.tw_full = plan->tw_full;
   prm.mel = plan->mel;
   prm.mel_w = plan->mel_w;
+  prm.tw_half4 = plan->tw_half4;
+  prm.tw_full4 = plan->tw_full4;
+  prm.mel_w2 = plan->mel_w2;
   prm.err = plan->err;
 
   const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
+  prm.x2 = plan->x2;
   void* args[] = {&prm};
-  cudaError_t e = cudaLaunchKernel(v->fn, dim3((unsigned)grid), dim3(v->threads), args, plan->smem,
-                                   reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = cudaLaunchKernel(v->fn, dim3((unsigned)grid), dim3(v->threads), args, plan->smem,
+                                         reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 

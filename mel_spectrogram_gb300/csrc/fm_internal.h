@@ -33,6 +33,12 @@ struct KernelParams {
   const float2* tw_full;  // W_{n_fft}^k, k <= n_fft/2, stored (cos, -sin)
   const int4* mel;        // n_mels x {start, len, offset, 0}
   const float* mel_w;     // nnz
+  // the same twiddles and weights duplicated for packed (two-frame) math:
+  // {c, c, d, d} for W = c + i d, and {w, w}
+  const float4* tw_half4;
+  const float4* tw_full4;
+  const float2* mel_w2;
+  const struct X2Tables* x2;  // two-frames-per-thread kernel only
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
 };
 
@@ -69,6 +75,43 @@ __host__ __device__ inline SmemLayout smem_layout(int n_fft, int hop, int n_mels
   return L;
 }
 
+// Constant tables of the two-frames-per-thread kernel, in one device block
+// that each CTA copies into shared memory. Sized for n_fft <= 400 (M <= 200):
+// every bin lies in at most two triangles, so nnz <= 2 (M + 1).
+constexpr int kX2MaxM = 200;
+constexpr int kX2MaxMels = 256;
+constexpr int kX2MaxNnz = 2 * (kX2MaxM + 1);
+struct X2Tables {
+  float4 p1[kX2MaxM];        // as KernelParams::p1
+  float4 tw_half[kX2MaxM];   // {c, c, d, d}, W_M^j = c + i d
+  float4 tw_full[kX2MaxM + 1];
+  int4 mel[kX2MaxMels];      // {start, len, offset, 0}
+  float2 mel_w[kX2MaxNnz];   // {w, w}
+};
+
+// Layout of the two-frames-per-thread kernel (32-frame tiles): its tables
+// (copied once per CTA from the X2Tables block), two input tiles (double
+// buffering) and the exchange buffer.
+struct SmemLayoutX2 {
+  size_t p1, tw_half, tw_full, mel, mel_w, in_tile, in_tile_bytes, xbuf, total;
+};
+
+__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n_mels, int nnz, int in_esize) {
+  const int M = n_fft / 2;
+  SmemLayoutX2 L;
+  size_t o = 0;
+  L.p1 = o;        o = align16(o + sizeof(float4) * M);
+  L.tw_half = o;   o = align16(o + sizeof(float4) * M);
+  L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));
+  L.mel = o;       o = align16(o + sizeof(int4) * n_mels);
+  L.mel_w = o;     o = align16(o + sizeof(float2) * (nnz > 0 ? nnz : 1));
+  L.in_tile_bytes = align16((size_t)in_esize * in_rows(n_fft, hop, 32) * in_row_stride(hop));
+  L.in_tile = o;   o += 2 * L.in_tile_bytes;
+  L.xbuf = o;      o = align16(o + sizeof(float4) * 16 * (size_t)(M + 1));
+  L.total = o;
+  return L;
+}
+
 // One compiled kernel: a fixed n_fft and its FFT split M = P * Q.
 struct Variant {
   int n_fft;
@@ -76,6 +119,7 @@ struct Variant {
   int frames_per_tile;  // G: frames per tile = lanes per role
   int threads;          // P * G
   int in_buffers;       // 2: the next tile's input lands while this one computes
+  int kind;             // 0: one frame per thread; 1: two frames per thread (packed)
   const void* fn;       // __global__ void(KernelParams)
 };
 

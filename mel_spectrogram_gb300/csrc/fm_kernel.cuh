@@ -69,33 +69,52 @@ __device__ __forceinline__ Raw raw_zero() {
 }
 
 // Stage rows [0, rows) of hop samples starting at signal index gstart of
-// signal row `src` (length T) into dst (row stride S elements). Returns true
-// if cp.async copies were issued (the caller commits and waits for them).
+// signal row `src` (length T) into dst (row stride S elements), as
+// asynchronous copies wherever possible: aligned in-range sample pairs as one
+// 8- or 4-byte cp.async; otherwise element by element, mirrored about the
+// first/last sample (reflect padding), f32 still by 4-byte cp.async and
+// 16-bit samples by plain loads (only the few mirrored or misaligned ones).
+// Positions past the padded signal are zero (no valid frame reads them).
+// The caller commits the group, waits for it and then synchronises the CTA.
 template <typename Raw, int NWARPS>
-__device__ __forceinline__ bool stage_tile(const Raw* __restrict__ src, long long T, long long gstart, int rows,
+__device__ __forceinline__ void stage_tile(const Raw* __restrict__ src, long long T, long long gstart, int rows,
                                            int hop, int S, Raw* dst, int warp, int lane) {
   const bool interior = gstart >= 0 && gstart + (long long)rows * hop <= T;
   const bool aligned = ((reinterpret_cast<uintptr_t>(src + gstart)) % (2 * sizeof(Raw))) == 0;
+  const int pairs = hop / 2;
   if (interior && aligned) {
-    const int pairs = hop / 2;
     for (int r = warp; r < rows; r += NWARPS) {
       const Raw* s = src + gstart + (long long)r * hop;
       Raw* d = dst + r * S;
       for (int c2 = lane; c2 < pairs; c2 += 32) cp_async<2 * sizeof(Raw)>(d + 2 * c2, s + 2 * c2);
     }
-    return true;
+    return;
   }
   for (int r = warp; r < rows; r += NWARPS) {
     Raw* d = dst + r * S;
     const long long s0 = gstart + (long long)r * hop;
-    for (int c = lane; c < hop; c += 32) {
-      long long s = s0 + c;
-      if (s < 0) s = -s;                   // mirror about the first sample
-      else if (s >= T) s = 2 * T - 2 - s;  // mirror about the last sample
-      d[c] = (s >= 0 && s < T) ? load_one(src + s) : raw_zero<Raw>();  // beyond the padded signal: unused
+    for (int c2 = lane; c2 < pairs; c2 += 32) {
+      const long long s = s0 + 2 * c2;
+      if (aligned && s >= 0 && s + 1 < T) {
+        cp_async<2 * sizeof(Raw)>(d + 2 * c2, src + s);
+        continue;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        long long se = s + e;
+        if (se < 0) se = -se;                   // mirror about the first sample
+        else if (se >= T) se = 2 * T - 2 - se;  // mirror about the last sample
+        Raw* de = d + 2 * c2 + e;
+        if (se < 0 || se >= T) {
+          *de = raw_zero<Raw>();
+        } else if constexpr (sizeof(Raw) == 4) {
+          cp_async<4>(de, src + se);
+        } else {
+          *de = load_one(src + se);
+        }
+      }
     }
   }
-  return false;
 }
 
 // Pass 1 for role p and frame g: windowed Q-point DFT of z[p + P q] and the
@@ -117,6 +136,45 @@ __device__ __forceinline__ void pass1(const Raw* __restrict__ frame_base, const 
 #pragma unroll
   for (int k2 = 1; k2 < Q; ++k2) xrow[k2 * P + p] = cmul(z[k2], s_twh[p * k2]);
 }
+
+// Copy `bytes` (a multiple of 8, both ends 8-byte aligned) from global to
+// shared memory with cp.async, 16 bytes per copy where alignment allows.
+__device__ __forceinline__ void copy_table_async(void* dst, const void* src, int bytes, int tid, int nthreads) {
+  unsigned char* d = static_cast<unsigned char*>(dst);
+  const unsigned char* s = static_cast<const unsigned char*>(src);
+  if (((reinterpret_cast<uintptr_t>(d) | reinterpret_cast<uintptr_t>(s)) & 15) == 0 && (bytes & 15) == 0) {
+    for (int i = tid * 16; i < bytes; i += nthreads * 16) cp_async<16>(d + i, s + i);
+  } else {
+    for (int i = tid * 8; i < bytes; i += nthreads * 8) cp_async<8>(d + i, s + i);
+  }
+}
+
+// tile -> (signal b, tile index within the signal), without a 64-bit divide:
+// a float reciprocal gives the quotient to within one, then one correction.
+struct TileSplitter {
+  int tps;
+  float inv;
+  __device__ explicit TileSplitter(int tiles_per_signal) : tps(tiles_per_signal), inv(1.0f / (float)tiles_per_signal) {}
+  __device__ __forceinline__ void operator()(long long tile, long long& b, int& tt) const {
+    if (tile < (1LL << 22)) {
+      const int t = (int)tile;
+      int q = (int)((float)t * inv);
+      int r = t - q * tps;
+      if (r < 0) {
+        r += tps;
+        --q;
+      } else if (r >= tps) {
+        r -= tps;
+        ++q;
+      }
+      b = q;
+      tt = r;
+    } else {
+      b = tile / tps;
+      tt = (int)(tile - b * tps);
+    }
+  }
+};
 
 template <int MODE>
 __device__ __forceinline__ float power_of(float2 x, float p) {
@@ -277,13 +335,15 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
   const int hop = prm.hop, S = in_row_stride(hop), rows = in_rows(N, hop, G);
   const Raw* in = static_cast<const Raw*>(prm.in);
   const long long T = prm.T;
-  const int tps = prm.tiles_per_signal;
+  const TileSplitter split(prm.tiles_per_signal);
   auto in_buf = [&](int i) { return reinterpret_cast<Raw*>(smem + lay.in_tile + (size_t)i * lay.in_tile_bytes); };
   auto stage = [&](long long tile, int buf) {
-    const long long b = tile / tps;
-    const long long t0 = (tile - b * tps) * (long long)G;
-    if (stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.pad, rows, hop, S, in_buf(buf), warp, lane))
-      cp_async_commit();
+    long long b;
+    int tt;
+    split(tile, b, tt);
+    const long long t0 = (long long)tt * G;
+    stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.pad, rows, hop, S, in_buf(buf), warp, lane);
+    cp_async_commit();
   };
 
   long long tile = blockIdx.x;
@@ -308,8 +368,10 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
     }
     __syncthreads();
 
-    const long long b = tile / tps;
-    const int t0 = (int)(tile - b * tps) * G;
+    long long b;
+    int tt;
+    split(tile, b, tt);
+    const int t0 = tt * G;
     const int n_valid = min(G, prm.n_frames - t0);
     const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
     if (prm.out_dtype == FM_F32)
@@ -322,6 +384,7 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
     // The next iteration's barrier orders these power-tile reads before the
     // next pass 1 overwrites the exchange buffer.
   }
+  cp_async_commit();  // nothing may stay in flight past the end of the CTA
   cp_async_wait_all();
 }
 
@@ -336,15 +399,14 @@ __global__ void __launch_bounds__(P* G) mel_kernel(const KernelParams prm) {
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
   const SmemLayout lay = smem_layout(N, prm.hop, prm.n_mels, prm.nnz, G, esize, NBUF);
 
-  // per-CTA constant tables, loaded once (the grid is persistent)
+  // per-CTA constant tables, fetched once (the grid is persistent) in the same
+  // cp.async group as the first tile, so one wait covers both
   const int tid = threadIdx.x;
-  for (int i = tid; i < M; i += THREADS) {
-    reinterpret_cast<float4*>(smem + lay.p1)[i] = prm.p1[i];
-    reinterpret_cast<float2*>(smem + lay.tw_half)[i] = prm.tw_half[i];
-  }
-  for (int i = tid; i <= M; i += THREADS) reinterpret_cast<float2*>(smem + lay.tw_full)[i] = prm.tw_full[i];
-  for (int i = tid; i < prm.n_mels; i += THREADS) reinterpret_cast<int4*>(smem + lay.mel)[i] = prm.mel[i];
-  for (int i = tid; i < prm.nnz; i += THREADS) reinterpret_cast<float*>(smem + lay.mel_w)[i] = prm.mel_w[i];
+  copy_table_async(smem + lay.p1, prm.p1, (int)sizeof(float4) * M, tid, THREADS);
+  copy_table_async(smem + lay.tw_half, prm.tw_half, (int)sizeof(float2) * M, tid, THREADS);
+  copy_table_async(smem + lay.tw_full, prm.tw_full, (int)sizeof(float2) * (M + 1) + ((M + 1) & 1) * 8, tid, THREADS);
+  copy_table_async(smem + lay.mel, prm.mel, (int)sizeof(int4) * prm.n_mels, tid, THREADS);
+  copy_table_async(smem + lay.mel_w, prm.mel_w, (int)align16(sizeof(float) * (prm.nnz > 0 ? prm.nnz : 1)), tid, THREADS);
   // (the first barrier inside run_tiles publishes the tables)
 
   if (prm.in_dtype == FM_F32) run_tiles<N, P, Q, G, NBUF, float>(prm, smem, lay);
@@ -358,5 +420,5 @@ __global__ void __launch_bounds__(P* G) mel_kernel(const KernelParams prm) {
 #define FM_DEFINE_VARIANT(NAME, N, P, Q, G, NBUF)                                                       \
   namespace fm {                                                                                        \
   template __global__ void mel_kernel<N, P, Q, G, NBUF>(const KernelParams);                          \
-  extern const Variant NAME = {N, P, Q, G, P * G, NBUF, (const void*)&mel_kernel<N, P, Q, G, NBUF>}; \
+  extern const Variant NAME = {N, P, Q, G, P * G, NBUF, 0, (const void*)&mel_kernel<N, P, Q, G, NBUF>}; \
   }

@@ -1,0 +1,244 @@
+// Two-frames-per-thread variant of the fused mel kernel (sm_103a), for the
+// splits with Q = 2P (n_fft = 400, 256, 64).
+//
+// Same path and same four-step real FFT as fm_kernel.cuh, but a tile holds 32
+// frames and thread (role, g), g < 16, carries frames g and g + 16 through
+// every phase as packed pairs (see fm_fft2.cuh):
+//   staging : raw samples as rows of `hop` (cp.async, double-buffered: the
+//             next tile lands while this one computes);
+//   tables  : window/offset, twiddles and filters are copied once per CTA
+//             into shared memory and read as broadcasts;
+//   pass 1  : two LDS.64 pair loads per step, the window multiply scatters
+//             them into the packed layout; Q-point DFT; twiddle W_M^{p k2};
+//             one 16-byte store {re_a, re_b, im_a, im_b} per value;
+//   pass 2  : P-point DFTs for k2 = t and Q - t (role 0: 0 and Q/2), then the
+//             real-FFT split and |X|^p, still packed;
+//   power   : tile P[k][g] = (frame g, frame g + 16);
+//   mel     : lane = frame pair, half-warps on two filters, one packed FMA
+//             per filter weight for both frames.
+#pragma once
+
+#include "fm_fft2.cuh"
+#include "fm_kernel.cuh"
+
+namespace fm {
+
+constexpr int kX2Lanes = 16;   // lanes per role
+constexpr int kX2Frames = 32;  // frames per tile
+
+template <int P, int Q, typename Raw>
+__device__ __forceinline__ void pass1_x2(const Raw* __restrict__ base_a, int S, const float4* __restrict__ s_p1,
+                                         const float4* __restrict__ s_twh4, float4* xq_row, int p) {
+  const Raw* base_b = base_a + kX2Lanes * S;
+  cx2 z[Q];
+  const float4* tab = s_p1 + p * Q;
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    const float4 e = tab[q];
+    const int off = __float_as_int(e.z);
+    const float2 va = load_pair(base_a + off);
+    const float2 vb = load_pair(base_b + off);
+    z[q].re = make_float2(va.x * e.x, vb.x * e.x);
+    z[q].im = make_float2(va.y * e.y, vb.y * e.y);
+  }
+  dft<Q>(z);
+  xq_row[p] = make_float4(z[0].re.x, z[0].re.y, z[0].im.x, z[0].im.y);
+#pragma unroll
+  for (int k2 = 1; k2 < Q; ++k2) {
+    const float4 w = s_twh4[p * k2];
+    const cx2 v = cmul(z[k2], make_float2(w.x, w.y), make_float2(w.z, w.w));
+    xq_row[k2 * P + p] = make_float4(v.re.x, v.re.y, v.im.x, v.im.y);
+  }
+}
+
+__device__ __forceinline__ cx2 load_cx2(const float4* p) {
+  const float4 v = *p;
+  return {make_float2(v.x, v.y), make_float2(v.z, v.w)};
+}
+
+template <int MODE>
+__device__ __forceinline__ float2 power2(float2 re, float2 im, float pw) {
+  const float2 m2 = fma2(re, re, mul2(im, im));
+  if constexpr (MODE == 0) return m2;
+  else if constexpr (MODE == 1) return make_float2(sqrtf(m2.x), sqrtf(m2.y));
+  else return make_float2(powf(m2.x, 0.5f * pw), powf(m2.y, 0.5f * pw));
+}
+
+// (|X[k]|^p, |X[M-k]|^p) for both frames from Z[k], Z[M-k] and W_N^k.
+template <int MODE>
+__device__ __forceinline__ void split_pair_x2(cx2 zk, cx2 zm, float4 w, float pw, float2& out_k, float2& out_mk) {
+  const cx2 s = {add2(zk.re, zm.re), sub2(zk.im, zm.im)};
+  const cx2 d = {sub2(zk.re, zm.re), add2(zk.im, zm.im)};
+  const cx2 v = cmul(d, make_float2(w.x, w.y), make_float2(w.z, w.w));
+  // X[k] = s - i v, conj X[M-k] = s + i v
+  out_k = power2<MODE>(add2(s.re, v.im), sub2(s.im, v.re), pw);
+  out_mk = power2<MODE>(sub2(s.re, v.im), add2(s.im, v.re), pw);
+}
+
+// Pass 2 and split for Q = 2P; power pairs go to pw_col[k * 16] (float2).
+template <int N, int P, int Q, int MODE>
+__device__ __forceinline__ void pass2_split_x2(const float4* xq_row, float2* pw_col, const float4* __restrict__ s_twf4,
+                                               int t, float pw) {
+  constexpr int M = N / 2;
+  static_assert(Q == 2 * P && P % 2 == 0, "paired split needs Q = 2P with P even");
+  const int kA = t;
+  const int kB = (t == 0) ? Q / 2 : Q - t;
+  cx2 a[P], b[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    a[p] = load_cx2(xq_row + kA * P + p);
+    b[p] = load_cx2(xq_row + kB * P + p);
+  }
+  dft<P>(a);  // a[k1] = Z[kA + Q k1]
+  dft<P>(b);  // b[k1] = Z[kB + Q k1]
+  __syncthreads();  // every exchange read is done: the power tile may overwrite it
+  if (t != 0) {
+#pragma unroll
+    for (int k1 = 0; k1 < P; ++k1) {
+      const int k = t + Q * k1;
+      float2 lo, hi;
+      split_pair_x2<MODE>(a[k1], b[P - 1 - k1], s_twf4[k], pw, lo, hi);
+      pw_col[k * kX2Lanes] = lo;
+      pw_col[(M - k) * kX2Lanes] = hi;
+    }
+  } else {
+#pragma unroll
+    for (int k1 = 0; k1 <= P / 2; ++k1) {
+      const int k = Q * k1;
+      float2 lo, hi;
+      split_pair_x2<MODE>(a[k1], a[(P - k1) % P], s_twf4[k], pw, lo, hi);
+      pw_col[k * kX2Lanes] = lo;
+      pw_col[(M - k) * kX2Lanes] = hi;
+    }
+#pragma unroll
+    for (int k1 = 0; k1 < P / 2; ++k1) {
+      const int k = Q / 2 + Q * k1;
+      float2 lo, hi;
+      split_pair_x2<MODE>(b[k1], b[P - 1 - k1], s_twf4[k], pw, lo, hi);
+      pw_col[k * kX2Lanes] = lo;
+      pw_col[(M - k) * kX2Lanes] = hi;
+    }
+  }
+}
+
+// Mel projection: lane g of each half-warp takes frames g and g + 16 of one
+// filter; the weight is read as a duplicated pair and applied with one packed
+// FMA. Stores: 16 consecutive frames per half-warp, twice.
+template <int NWARPS, typename OutT>
+__device__ __forceinline__ void mel_project_x2(const float2* s_pw2, const int4* __restrict__ s_mel,
+                                               const float2* __restrict__ s_mw2, OutT* out_tile, int n_valid,
+                                               int n_mels, long long n_frames, int warp, int lane) {
+  const int g = lane & 15, sub = lane >> 4;
+  const float2* pcol = s_pw2 + g;
+  const bool va = g < n_valid, vb = g + kX2Lanes < n_valid;
+  for (int m = warp * 2 + sub; m < n_mels; m += NWARPS * 2) {
+    const int4 md = s_mel[m];
+    const float2* pr = pcol + md.x * kX2Lanes;
+    const float2* wr = s_mw2 + md.z;
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll 2
+    for (int j = 0; j < md.y; ++j) acc = fma2(wr[j], pr[j * kX2Lanes], acc);
+    OutT* o = out_tile + (long long)m * n_frames + g;
+    if (va) store_out(o, acc.x);
+    if (vb) store_out(o + kX2Lanes, acc.y);
+  }
+}
+
+template <int N, int P, int Q, typename Raw>
+__device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay) {
+  constexpr int M = N / 2;
+  constexpr int THREADS = P * kX2Lanes;
+  constexpr int NWARPS = THREADS / 32;
+  constexpr int GS4 = M + 1;  // float4 stride between frame pairs in the exchange buffer (odd)
+  const float4* s_p1 = reinterpret_cast<const float4*>(smem + lay.p1);
+  const float4* s_twh4 = reinterpret_cast<const float4*>(smem + lay.tw_half);
+  const float4* s_twf4 = reinterpret_cast<const float4*>(smem + lay.tw_full);
+  const int4* s_mel = reinterpret_cast<const int4*>(smem + lay.mel);
+  const float2* s_mw2 = reinterpret_cast<const float2*>(smem + lay.mel_w);
+  float4* s_xq = reinterpret_cast<float4*>(smem + lay.xbuf);
+  float2* s_pw2 = reinterpret_cast<float2*>(smem + lay.xbuf);  // aliases s_xq after pass 2
+  auto in_buf = [&](int i) { return reinterpret_cast<Raw*>(smem + lay.in_tile + (size_t)i * lay.in_tile_bytes); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = tid % kX2Lanes, role = tid / kX2Lanes;
+  const int hop = prm.hop, S = in_row_stride(hop), rows = in_rows(N, hop, kX2Frames);
+  const Raw* in = static_cast<const Raw*>(prm.in);
+  const long long T = prm.T;
+  const TileSplitter split(prm.tiles_per_signal);
+  auto stage = [&](long long tile, int buf) {
+    long long b;
+    int tt;
+    split(tile, b, tt);
+    const long long t0 = (long long)tt * kX2Frames;
+    stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.pad, rows, hop, S, in_buf(buf), warp, lane);
+    cp_async_commit();
+  };
+
+  long long tile = blockIdx.x;
+  int buf = 0;
+  if (tile < prm.total_tiles) stage(tile, 0);
+  for (; tile < prm.total_tiles; tile += gridDim.x, buf ^= 1) {
+    cp_async_wait_all();
+    __syncthreads();  // this tile's samples are visible; the previous tile is fully done
+    const long long next = tile + gridDim.x;
+    if (next < prm.total_tiles) stage(next, buf ^ 1);  // lands while this tile computes
+
+    float4* xq_row = s_xq + g * GS4;
+    pass1_x2<P, Q, Raw>(in_buf(buf) + g * S, S, s_p1, s_twh4, xq_row, role);
+    __syncthreads();
+
+    switch (prm.power_mode) {
+      case 0: pass2_split_x2<N, P, Q, 0>(xq_row, s_pw2 + g, s_twf4, role, prm.power); break;
+      case 1: pass2_split_x2<N, P, Q, 1>(xq_row, s_pw2 + g, s_twf4, role, prm.power); break;
+      default: pass2_split_x2<N, P, Q, 2>(xq_row, s_pw2 + g, s_twf4, role, prm.power); break;
+    }
+    __syncthreads();
+
+    long long b;
+    int tt;
+    split(tile, b, tt);
+    const int t0 = tt * kX2Frames;
+    const int n_valid = min(kX2Frames, prm.n_frames - t0);
+    const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
+    if (prm.out_dtype == FM_F32)
+      mel_project_x2<NWARPS>(s_pw2, s_mel, s_mw2, static_cast<float*>(prm.out) + obase, n_valid, prm.n_mels,
+                             prm.n_frames, warp, lane);
+    else
+      mel_project_x2<NWARPS>(s_pw2, s_mel, s_mw2, static_cast<__half*>(prm.out) + obase, n_valid, prm.n_mels,
+                             prm.n_frames, warp, lane);
+  }
+  cp_async_commit();  // nothing may stay in flight past the end of the CTA
+  cp_async_wait_all();
+}
+
+template <int N, int P, int Q>
+__global__ void __launch_bounds__(P* kX2Lanes) mel_kernel_x2(const KernelParams prm) {
+  constexpr int M = N / 2;
+  constexpr int THREADS = P * kX2Lanes;
+  static_assert(P * Q == M && Q == 2 * P && M <= kX2MaxM, "x2 kernel needs Q = 2P and M <= 200");
+  static_assert(THREADS % 32 == 0, "CTA must be whole warps");
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
+  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, prm.n_mels, prm.nnz, esize);
+  // tables, fetched once per CTA in the first tile's cp.async group
+  const int tid = threadIdx.x;
+  const X2Tables* t = prm.x2;
+  copy_table_async(smem + lay.p1, t->p1, (int)sizeof(float4) * M, tid, THREADS);
+  copy_table_async(smem + lay.tw_half, t->tw_half, (int)sizeof(float4) * M, tid, THREADS);
+  copy_table_async(smem + lay.tw_full, t->tw_full, (int)sizeof(float4) * (M + 1), tid, THREADS);
+  copy_table_async(smem + lay.mel, t->mel, (int)sizeof(int4) * prm.n_mels, tid, THREADS);
+  copy_table_async(smem + lay.mel_w, t->mel_w, (int)sizeof(float2) * ((prm.nnz + 1) & ~1), tid, THREADS);
+  if (prm.in_dtype == FM_F32) run_tiles_x2<N, P, Q, float>(prm, smem, lay);
+  else if (prm.in_dtype == FM_I16) run_tiles_x2<N, P, Q, short>(prm, smem, lay);
+  else run_tiles_x2<N, P, Q, __half>(prm, smem, lay);
+}
+
+}  // namespace fm
+
+// Instantiate one two-frames-per-thread variant: FM_DEFINE_VARIANT_X2(name, N, P, Q)
+#define FM_DEFINE_VARIANT_X2(NAME, N, P, Q)                                                   \
+  namespace fm {                                                                              \
+  template __global__ void mel_kernel_x2<N, P, Q>(const KernelParams);                       \
+  extern const Variant NAME = {N, P, Q, kX2Frames, P * kX2Lanes, 1, 1,                         \
+                               (const void*)&mel_kernel_x2<N, P, Q>};                          \
+  }
