@@ -39,6 +39,7 @@ struct KernelParams {
   const float4* tw_full4;
   const float2* mel_w2;
   const struct X2Tables* x2;  // two-frames-per-thread kernel only
+  int x2_chunks, x2_w;        // its mel chunk count and padded weight-pair count
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
 };
 
@@ -80,31 +81,44 @@ __host__ __device__ inline SmemLayout smem_layout(int n_fft, int hop, int n_mels
 // every bin lies in at most two triangles, so nnz <= 2 (M + 1).
 constexpr int kX2MaxM = 200;
 constexpr int kX2MaxMels = 256;
-constexpr int kX2MaxNnz = 2 * (kX2MaxM + 1);
+constexpr int kX2MaxW = 2 * (kX2MaxM + 1) + 4 * kX2MaxMels + 2;  // padded weight pairs
+constexpr int kX2MaxWarps = 16;
+constexpr int kX2Unroll = 4;  // chunks per unrolled mel iteration
+constexpr int kX2MaxChunks = kX2MaxW / 2 + kX2Unroll * kX2MaxWarps;
+enum { kChunkFirst = 1, kChunkLast = 2 };
 struct X2Tables {
   float4 p1[kX2MaxM];        // as KernelParams::p1
   float4 tw_half[kX2MaxM];   // {c, c, d, d}, W_M^j = c + i d
   float4 tw_full[kX2MaxM + 1];
-  int4 mel[kX2MaxMels];      // {start, len, offset, 0}
-  float2 mel_w[kX2MaxNnz];   // {w, w}
+  // Mel work as a stream of chunks. Filters 2i and 2i+1 (one per half-warp)
+  // are padded to one even length L >= 2 and cut into L/2 chunks of two
+  // bins; each warp runs its chunks [warp_begin[w], warp_begin[w + 1]), a
+  // multiple of kX2Unroll long (padded with no-op chunks). chunk[c][h] =
+  // {byte offset of the chunk's first bin in a lane's power column
+  // (bin * 128), byte offset of its two weight pairs (16-byte aligned),
+  // filter index, flags (kChunkFirst: start a sum, kChunkLast: store it)}.
+  int warp_begin[kX2MaxWarps + 1];
+  int4 chunk[kX2MaxChunks][2];
+  float2 mel_w[kX2MaxW];     // {w, w}; zeros where a filter was padded
 };
 
 // Layout of the two-frames-per-thread kernel (32-frame tiles): its tables
 // (copied once per CTA from the X2Tables block), two input tiles (double
 // buffering) and the exchange buffer.
 struct SmemLayoutX2 {
-  size_t p1, tw_half, tw_full, mel, mel_w, in_tile, in_tile_bytes, xbuf, total;
+  size_t p1, tw_half, tw_full, chunks, mel_w, in_tile, in_tile_bytes, xbuf, total;
 };
 
-__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n_mels, int nnz, int in_esize) {
+// n_chunks: mel chunks (int4 x 2 each); n_w: padded weight pairs
+__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n_chunks, int n_w, int in_esize) {
   const int M = n_fft / 2;
   SmemLayoutX2 L;
   size_t o = 0;
   L.p1 = o;        o = align16(o + sizeof(float4) * M);
   L.tw_half = o;   o = align16(o + sizeof(float4) * M);
   L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));
-  L.mel = o;       o = align16(o + sizeof(int4) * n_mels);
-  L.mel_w = o;     o = align16(o + sizeof(float2) * (nnz > 0 ? nnz : 1));
+  L.chunks = o;    o = align16(o + sizeof(int4) * 2 * (n_chunks > 0 ? n_chunks : 1));
+  L.mel_w = o;     o = align16(o + sizeof(float2) * (n_w > 0 ? n_w : 2));
   L.in_tile_bytes = align16((size_t)in_esize * in_rows(n_fft, hop, 32) * in_row_stride(hop));
   L.in_tile = o;   o += 2 * L.in_tile_bytes;
   L.xbuf = o;      o = align16(o + sizeof(float4) * 16 * (size_t)(M + 1));

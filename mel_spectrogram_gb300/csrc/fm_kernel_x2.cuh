@@ -121,26 +121,44 @@ __device__ __forceinline__ void pass2_split_x2(const float4* xq_row, float2* pw_
   }
 }
 
-// Mel projection: lane g of each half-warp takes frames g and g + 16 of one
-// filter; the weight is read as a duplicated pair and applied with one packed
-// FMA. Stores: 16 consecutive frames per half-warp, twice.
-template <int NWARPS, typename OutT>
-__device__ __forceinline__ void mel_project_x2(const float2* s_pw2, const int4* __restrict__ s_mel,
+// Mel projection over this warp's chunk stream (see X2Tables). Each chunk
+// adds two bins of one filter per half-warp: lane g takes frames g and g + 16
+// as a packed pair, the two weights arrive as one 16-byte broadcast of
+// duplicated pairs. Chunk flags start a sum and store it, so the loop has no
+// data-dependent bounds and runs kX2Unroll chunks per iteration with all
+// their loads in flight. Stores: 16 consecutive frames per half-warp, twice.
+template <typename OutT>
+__device__ __forceinline__ void mel_project_x2(const float2* s_pw2, const int4* __restrict__ s_chunks,
                                                const float2* __restrict__ s_mw2, OutT* out_tile, int n_valid,
-                                               int n_mels, long long n_frames, int warp, int lane) {
-  const int g = lane & 15, sub = lane >> 4;
-  const float2* pcol = s_pw2 + g;
+                                               long long n_frames, int c_begin, int c_end, int lane) {
+  const int g = lane & 15, h = lane >> 4;
+  const char* pcol = reinterpret_cast<const char*>(s_pw2 + g);
+  const char* wbase = reinterpret_cast<const char*>(s_mw2);
   const bool va = g < n_valid, vb = g + kX2Lanes < n_valid;
-  for (int m = warp * 2 + sub; m < n_mels; m += NWARPS * 2) {
-    const int4 md = s_mel[m];
-    const float2* pr = pcol + md.x * kX2Lanes;
-    const float2* wr = s_mw2 + md.z;
-    float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll 2
-    for (int j = 0; j < md.y; ++j) acc = fma2(wr[j], pr[j * kX2Lanes], acc);
-    OutT* o = out_tile + (long long)m * n_frames + g;
-    if (va) store_out(o, acc.x);
-    if (vb) store_out(o + kX2Lanes, acc.y);
+  float2 acc = make_float2(0.0f, 0.0f);
+  for (int c = c_begin; c < c_end; c += kX2Unroll) {
+    int4 d[kX2Unroll];
+    float4 w[kX2Unroll];
+    float2 p0[kX2Unroll], p1[kX2Unroll];
+#pragma unroll
+    for (int u = 0; u < kX2Unroll; ++u) d[u] = s_chunks[2 * (c + u) + h];
+#pragma unroll
+    for (int u = 0; u < kX2Unroll; ++u) {
+      w[u] = *reinterpret_cast<const float4*>(wbase + d[u].y);
+      p0[u] = *reinterpret_cast<const float2*>(pcol + d[u].x);
+      p1[u] = *reinterpret_cast<const float2*>(pcol + d[u].x + kX2Lanes * (int)sizeof(float2));
+    }
+#pragma unroll
+    for (int u = 0; u < kX2Unroll; ++u) {
+      if (d[u].w & kChunkFirst) acc = make_float2(0.0f, 0.0f);
+      acc = fma2(make_float2(w[u].x, w[u].y), p0[u], acc);
+      acc = fma2(make_float2(w[u].z, w[u].w), p1[u], acc);
+      if (d[u].w & kChunkLast) {
+        OutT* o = out_tile + (long long)d[u].z * n_frames + g;
+        if (va) store_out(o, acc.x);
+        if (vb) store_out(o + kX2Lanes, acc.y);
+      }
+    }
   }
 }
 
@@ -153,7 +171,7 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const float4* s_p1 = reinterpret_cast<const float4*>(smem + lay.p1);
   const float4* s_twh4 = reinterpret_cast<const float4*>(smem + lay.tw_half);
   const float4* s_twf4 = reinterpret_cast<const float4*>(smem + lay.tw_full);
-  const int4* s_mel = reinterpret_cast<const int4*>(smem + lay.mel);
+  const int4* s_chunks = reinterpret_cast<const int4*>(smem + lay.chunks);
   const float2* s_mw2 = reinterpret_cast<const float2*>(smem + lay.mel_w);
   float4* s_xq = reinterpret_cast<float4*>(smem + lay.xbuf);
   float2* s_pw2 = reinterpret_cast<float2*>(smem + lay.xbuf);  // aliases s_xq after pass 2
@@ -165,6 +183,7 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const Raw* in = static_cast<const Raw*>(prm.in);
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
+  const int s_begin = __ldg(&prm.x2->warp_begin[warp]), s_end = __ldg(&prm.x2->warp_begin[warp + 1]);
   auto stage = [&](long long tile, int buf) {
     long long b;
     int tt;
@@ -201,11 +220,11 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     const int n_valid = min(kX2Frames, prm.n_frames - t0);
     const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
     if (prm.out_dtype == FM_F32)
-      mel_project_x2<NWARPS>(s_pw2, s_mel, s_mw2, static_cast<float*>(prm.out) + obase, n_valid, prm.n_mels,
-                             prm.n_frames, warp, lane);
+      mel_project_x2(s_pw2, s_chunks, s_mw2, static_cast<float*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
+                     s_end, lane);
     else
-      mel_project_x2<NWARPS>(s_pw2, s_mel, s_mw2, static_cast<__half*>(prm.out) + obase, n_valid, prm.n_mels,
-                             prm.n_frames, warp, lane);
+      mel_project_x2(s_pw2, s_chunks, s_mw2, static_cast<__half*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
+                     s_end, lane);
   }
   cp_async_commit();  // nothing may stay in flight past the end of the CTA
   cp_async_wait_all();
@@ -219,15 +238,15 @@ __global__ void __launch_bounds__(P* kX2Lanes) mel_kernel_x2(const KernelParams 
   static_assert(THREADS % 32 == 0, "CTA must be whole warps");
   extern __shared__ __align__(16) unsigned char smem[];
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
-  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, prm.n_mels, prm.nnz, esize);
+  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, prm.x2_chunks, prm.x2_w, esize);
   // tables, fetched once per CTA in the first tile's cp.async group
   const int tid = threadIdx.x;
   const X2Tables* t = prm.x2;
   copy_table_async(smem + lay.p1, t->p1, (int)sizeof(float4) * M, tid, THREADS);
   copy_table_async(smem + lay.tw_half, t->tw_half, (int)sizeof(float4) * M, tid, THREADS);
   copy_table_async(smem + lay.tw_full, t->tw_full, (int)sizeof(float4) * (M + 1), tid, THREADS);
-  copy_table_async(smem + lay.mel, t->mel, (int)sizeof(int4) * prm.n_mels, tid, THREADS);
-  copy_table_async(smem + lay.mel_w, t->mel_w, (int)sizeof(float2) * ((prm.nnz + 1) & ~1), tid, THREADS);
+  copy_table_async(smem + lay.chunks, t->chunk, (int)sizeof(int4) * 2 * prm.x2_chunks, tid, THREADS);
+  copy_table_async(smem + lay.mel_w, t->mel_w, (int)sizeof(float2) * prm.x2_w, tid, THREADS);
   if (prm.in_dtype == FM_F32) run_tiles_x2<N, P, Q, float>(prm, smem, lay);
   else if (prm.in_dtype == FM_I16) run_tiles_x2<N, P, Q, short>(prm, smem, lay);
   else run_tiles_x2<N, P, Q, __half>(prm, smem, lay);
