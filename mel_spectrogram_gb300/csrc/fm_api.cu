@@ -222,7 +222,7 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   // pass-1 table: role p, step q -> window at 2n, 2n+1 (n = p + P q) and the
   // tile offset of sample 2n (rows of hop samples, stride in_row_stride)
   const int M = n_fft / 2;
-  const int S = fm::in_row_stride(hop);
+  const int S = var->kind == 1 ? fm::in_row_stride_x2(hop, in_esize) : fm::in_row_stride(hop);
   const float in_scale = in_dtype == FM_I16 ? 1.0f / 32768.0f : 1.0f;  // exact power of two
   std::vector<float4> p1(M);
   for (int pp = 0; pp < var->P; ++pp)

@@ -102,11 +102,21 @@ struct X2Tables {
   float2 mel_w[kX2MaxW];     // {w, w}; zeros where a filter was padded
 };
 
+// Row stride (elements) of the packed kernel's staged tile: each row starts
+// on a 16-byte boundary (TMA bulk copies need it) and the stride is an odd
+// multiple of 16 bytes, so the per-frame pair reads of 16 lanes spread over
+// 8 bank groups (two lanes per group).
+__host__ __device__ inline int in_row_stride_x2(int hop, int esize) {
+  const int per16 = 16 / esize;  // elements per 16 bytes
+  const int s = (hop + per16 - 1) / per16;
+  return (s | 1) * per16;
+}
+
 // Layout of the two-frames-per-thread kernel (32-frame tiles): its tables
 // (copied once per CTA from the X2Tables block), two input tiles (double
 // buffering) and the exchange buffer.
 struct SmemLayoutX2 {
-  size_t p1, tw_half, tw_full, chunks, mel_w, in_tile, in_tile_bytes, xbuf, total;
+  size_t bars, p1, tw_half, tw_full, chunks, mel_w, in_tile, in_tile_bytes, xbuf, total;
 };
 
 // n_chunks: mel chunks (int4 x 2 each); n_w: padded weight pairs
@@ -114,12 +124,13 @@ __host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n
   const int M = n_fft / 2;
   SmemLayoutX2 L;
   size_t o = 0;
+  L.bars = o;      o = align16(o + 2 * sizeof(unsigned long long));  // one mbarrier per input buffer
   L.p1 = o;        o = align16(o + sizeof(float4) * M);
   L.tw_half = o;   o = align16(o + sizeof(float4) * M);
   L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));
   L.chunks = o;    o = align16(o + sizeof(int4) * 2 * (n_chunks > 0 ? n_chunks : 1));
   L.mel_w = o;     o = align16(o + sizeof(float2) * (n_w > 0 ? n_w : 2));
-  L.in_tile_bytes = align16((size_t)in_esize * in_rows(n_fft, hop, 32) * in_row_stride(hop));
+  L.in_tile_bytes = align16((size_t)in_esize * in_rows(n_fft, hop, 32) * in_row_stride_x2(hop, in_esize));
   L.in_tile = o;   o += 2 * L.in_tile_bytes;
   L.xbuf = o;      o = align16(o + sizeof(float4) * 16 * (size_t)(M + 1));
   L.total = o;

@@ -4,8 +4,10 @@
 // Same path and same four-step real FFT as fm_kernel.cuh, but a tile holds 32
 // frames and thread (role, g), g < 16, carries frames g and g + 16 through
 // every phase as packed pairs (see fm_fft2.cuh):
-//   staging : raw samples as rows of `hop` (cp.async, double-buffered: the
-//             next tile lands while this one computes);
+//   staging : raw samples as rows of `hop`, double-buffered so the next tile
+//             lands while this one computes: TMA bulk copies (one per row,
+//             issued by warp 0, completing on an mbarrier) for interior tiles
+//             with 16-byte aligned rows, cp.async element copies otherwise;
 //   tables  : window/offset, twiddles and filters are copied once per CTA
 //             into shared memory and read as broadcasts;
 //   pass 1  : two LDS.64 pair loads per step, the window multiply scatters
@@ -175,30 +177,70 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const float2* s_mw2 = reinterpret_cast<const float2*>(smem + lay.mel_w);
   float4* s_xq = reinterpret_cast<float4*>(smem + lay.xbuf);
   float2* s_pw2 = reinterpret_cast<float2*>(smem + lay.xbuf);  // aliases s_xq after pass 2
-  auto in_buf = [&](int i) { return reinterpret_cast<Raw*>(smem + lay.in_tile + (size_t)i * lay.in_tile_bytes); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = tid % kX2Lanes, role = tid / kX2Lanes;
-  const int hop = prm.hop, S = in_row_stride(hop), rows = in_rows(N, hop, kX2Frames);
+  const int esize = (int)sizeof(Raw);
+  const int hop = prm.hop, S = in_row_stride_x2(hop, esize), rows = in_rows(N, hop, kX2Frames);
   const Raw* in = static_cast<const Raw*>(prm.in);
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
   const int s_begin = __ldg(&prm.x2->warp_begin[warp]), s_end = __ldg(&prm.x2->warp_begin[warp + 1]);
-  auto stage = [&](long long tile, int buf) {
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + lay.bars);
+  auto in_buf = [&](int i) { return reinterpret_cast<Raw*>(smem + lay.in_tile + (size_t)i * lay.in_tile_bytes); };
+  // Tile placement: signal index of tile position 0, and whether the tile is
+  // interior with 16-byte aligned rows (then TMA bulk copies stage it).
+  auto locate = [&](long long tile, long long& gstart, const Raw*& src) {
     long long b;
     int tt;
     split(tile, b, tt);
-    const long long t0 = (long long)tt * kX2Frames;
-    stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.pad, rows, hop, S, in_buf(buf), warp, lane);
+    gstart = (long long)tt * kX2Frames * hop - prm.pad;
+    src = in + b * T;
+    return gstart >= 0 && gstart + (long long)rows * hop <= T && ((hop * esize) & 15) == 0 &&
+           (reinterpret_cast<uintptr_t>(src + gstart) & 15) == 0;
+  };
+  // Stage a tile into buffer `buf`: TMA row copies issued by warp 0 (one row
+  // per lane), or cp.async element copies by all threads at the signal edges.
+  auto stage = [&](long long tile, int buf) {
+    long long gstart;
+    const Raw* src;
+    if (locate(tile, gstart, src)) {
+      if (warp == 0) {
+        if (lane == 0) {
+          fence_proxy_async();  // the buffer was last read through the generic proxy
+          mbar_arrive_expect_tx(&bars[buf], (unsigned)(rows * hop * esize));
+        }
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32)
+          tma_load_1d(in_buf(buf) + r * S, src + gstart + (long long)r * hop, (unsigned)(hop * esize), &bars[buf]);
+      }
+    } else {
+      stage_tile<Raw, NWARPS>(src, T, gstart, rows, hop, S, in_buf(buf), warp, lane);
+    }
     cp_async_commit();
   };
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();  // the barriers exist before anyone polls them
+  unsigned phase[2] = {0u, 0u};
 
   long long tile = blockIdx.x;
   int buf = 0;
   if (tile < prm.total_tiles) stage(tile, 0);
   for (; tile < prm.total_tiles; tile += gridDim.x, buf ^= 1) {
     cp_async_wait_all();
-    __syncthreads();  // this tile's samples are visible; the previous tile is fully done
+    long long gs;
+    const Raw* sp;
+    bool failed = false;
+    if (locate(tile, gs, sp)) {
+      failed = !mbar_wait_bounded(&bars[buf], phase[buf], prm.err);
+      phase[buf] ^= 1u;
+    }
+    // this tile's samples are visible; the previous tile is fully done
+    if (__syncthreads_or(failed)) return;  // a staging copy never arrived (error recorded)
     const long long next = tile + gridDim.x;
     if (next < prm.total_tiles) stage(next, buf ^ 1);  // lands while this tile computes
 
