@@ -32,13 +32,16 @@ from mel_spectrogram_gb300.workloads import WORKLOADS, make_input  # noqa: E402
 METRIC = "mel frames/sec and achieved HBM GB/s (fraction of roofline) at B=8×480000 fp32"
 BUFFER_SETS = 16
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCES = ["fm_kernel.cuh", "fm_internal.h", "fm_kernel_n400.cu", "fm_kernel_n1024.cu", "fm_kernel_n2048.cu"]
-
-
 def kernel_sha() -> str:
+    """Fingerprint of the device code (every kernel source and header)."""
+    import glob
+
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "mel_spectrogram_gb300", "csrc", f), "rb") as fh:
+    csrc = os.path.join(ROOT, "mel_spectrogram_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "fm_kernel*")) + glob.glob(os.path.join(csrc, "fm_fft*.cuh")) +
+                    [os.path.join(csrc, "fm_internal.h")]):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
 
