@@ -188,35 +188,43 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const int s_begin = __ldg(&prm.x2->warp_begin[warp]), s_end = __ldg(&prm.x2->warp_begin[warp + 1]);
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + lay.bars);
   auto in_buf = [&](int i) { return reinterpret_cast<Raw*>(smem + lay.in_tile + (size_t)i * lay.in_tile_bytes); };
-  // Tile placement: signal index of tile position 0, and whether the tile is
-  // interior with 16-byte aligned rows (then TMA bulk copies stage it).
-  auto locate = [&](long long tile, long long& gstart, const Raw*& src) {
-    long long b;
+  // Where a tile lives: signal b, tile index tt within it, signal index of
+  // tile position 0, and whether it is interior with 16-byte aligned rows
+  // (then TMA bulk copies stage it). Computed once per tile and carried.
+  struct Place {
+    long long b, gstart;
     int tt;
-    split(tile, b, tt);
-    gstart = (long long)tt * kX2Frames * hop - prm.pad;
-    src = in + b * T;
-    return gstart >= 0 && gstart + (long long)rows * hop <= T && ((hop * esize) & 15) == 0 &&
-           (reinterpret_cast<uintptr_t>(src + gstart) & 15) == 0;
+    bool tma;
+  };
+  auto locate = [&](long long tile) {
+    Place pl;
+    split(tile, pl.b, pl.tt);
+    pl.gstart = (long long)pl.tt * kX2Frames * hop - prm.pad;
+    const Raw* src = in + pl.b * T;
+    pl.tma = pl.gstart >= 0 && pl.gstart + (long long)rows * hop <= T && ((hop * esize) & 15) == 0 &&
+             (reinterpret_cast<uintptr_t>(src + pl.gstart) & 15) == 0;
+    return pl;
   };
   // Stage a tile into buffer `buf`: TMA row copies issued by warp 0 (one row
   // per lane), or cp.async element copies by all threads at the signal edges.
-  auto stage = [&](long long tile, int buf) {
-    long long gstart;
-    const Raw* src;
-    if (locate(tile, gstart, src)) {
+  // A buffer last filled by cp.async gets a proxy fence before TMA refills it.
+  unsigned filled_by_cp = 0u;  // bit b: buffer b was last filled by cp.async
+  auto stage = [&](const Place& pl, int buf) {
+    const Raw* src = in + pl.b * T;
+    if (pl.tma) {
       if (warp == 0) {
         if (lane == 0) {
-          fence_proxy_async();  // the buffer was last read through the generic proxy
+          if ((filled_by_cp >> buf) & 1u) fence_proxy_async();
           mbar_arrive_expect_tx(&bars[buf], (unsigned)(rows * hop * esize));
         }
         __syncwarp();
         for (int r = lane; r < rows; r += 32)
-          tma_load_1d(in_buf(buf) + r * S, src + gstart + (long long)r * hop, (unsigned)(hop * esize), &bars[buf]);
+          tma_load_1d(in_buf(buf) + r * S, src + pl.gstart + (long long)r * hop, (unsigned)(hop * esize), &bars[buf]);
       }
     } else {
-      stage_tile<Raw, NWARPS>(src, T, gstart, rows, hop, S, in_buf(buf), warp, lane);
+      stage_tile<Raw, NWARPS>(src, T, pl.gstart, rows, hop, S, in_buf(buf), warp, lane);
     }
+    filled_by_cp = (filled_by_cp & ~(1u << buf)) | ((pl.tma ? 0u : 1u) << buf);
     cp_async_commit();
   };
   if (tid == 0) {
@@ -225,24 +233,27 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     fence_mbar_init();
   }
   __syncthreads();  // the barriers exist before anyone polls them
-  unsigned phase[2] = {0u, 0u};
+  unsigned phase = 0u;  // bit b: parity of buffer b's next mbarrier phase
 
   long long tile = blockIdx.x;
   int buf = 0;
-  if (tile < prm.total_tiles) stage(tile, 0);
+  Place cur = locate(tile);
+  if (tile < prm.total_tiles) stage(cur, 0);
   for (; tile < prm.total_tiles; tile += gridDim.x, buf ^= 1) {
     cp_async_wait_all();
-    long long gs;
-    const Raw* sp;
     bool failed = false;
-    if (locate(tile, gs, sp)) {
-      failed = !mbar_wait_bounded(&bars[buf], phase[buf], prm.err);
-      phase[buf] ^= 1u;
+    if (cur.tma) {
+      failed = !mbar_wait_bounded(&bars[buf], (phase >> buf) & 1u, prm.err);
+      phase ^= 1u << buf;
     }
     // this tile's samples are visible; the previous tile is fully done
     if (__syncthreads_or(failed)) return;  // a staging copy never arrived (error recorded)
     const long long next = tile + gridDim.x;
-    if (next < prm.total_tiles) stage(next, buf ^ 1);  // lands while this tile computes
+    Place nxt{};
+    if (next < prm.total_tiles) {
+      nxt = locate(next);
+      stage(nxt, buf ^ 1);  // lands while this tile computes
+    }
 
     float4* xq_row = s_xq + g * GS4;
     pass1_x2<P, Q, Raw>(in_buf(buf) + g * S, S, s_p1, s_twh4, xq_row, role);
@@ -255,12 +266,10 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     }
     __syncthreads();
 
-    long long b;
-    int tt;
-    split(tile, b, tt);
-    const int t0 = tt * kX2Frames;
+    const int t0 = cur.tt * kX2Frames;
     const int n_valid = min(kX2Frames, prm.n_frames - t0);
-    const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
+    const long long obase = cur.b * prm.n_mels * (long long)prm.n_frames + t0;
+    cur = nxt;
     if (prm.out_dtype == FM_F32)
       mel_project_x2(s_pw2, s_chunks, s_mw2, static_cast<float*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
                      s_end, lane);
