@@ -15,14 +15,14 @@
 #include "fm_mel.h"
 
 namespace fm {
-extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant512, kVariant1024,
-    kVariant2048;
+extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant400h160, kVariant512,
+    kVariant1024, kVariant2048;
 
-const Variant* find_variant(int n_fft) {
-  static const Variant* all[] = {&kVariant64,  &kVariant128,  &kVariant256, &kVariant400,
-                                 &kVariant512, &kVariant1024, &kVariant2048};
+const Variant* find_variant(int n_fft, int hop) {
+  static const Variant* all[] = {&kVariant400h160, &kVariant64,  &kVariant128,  &kVariant256, &kVariant400,
+                                 &kVariant512,     &kVariant1024, &kVariant2048};
   for (const Variant* v : all)
-    if (v->n_fft == n_fft) return v;
+    if (v->n_fft == n_fft && (v->hop == 0 || v->hop == hop)) return v;
   return nullptr;
 }
 }  // namespace fm
@@ -151,7 +151,7 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   fm_status st = fm::check_filter_args(sr, n_fft, n_mels, f_min, &f_max, mel_scale, norm);
   if (st != FM_OK) return st;
   if (!fm::is_supported_nfft(n_fft) || n_mels > 256 || (hop % 2) != 0) return FM_ERR_UNSUPPORTED;
-  const fm::Variant* var = fm::find_variant(n_fft);
+  const fm::Variant* var = fm::find_variant(n_fft, hop);
   if (var == nullptr) return FM_ERR_UNSUPPORTED;
 
   // host tables (double precision, rounded to float)

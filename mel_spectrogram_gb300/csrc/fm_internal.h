@@ -106,17 +106,19 @@ struct X2Tables {
 // on a 16-byte boundary (TMA bulk copies need it) and the stride is an odd
 // multiple of 16 bytes, so the per-frame pair reads of 16 lanes spread over
 // 8 bank groups (two lanes per group).
-__host__ __device__ inline int in_row_stride_x2(int hop, int esize) {
-  const int per16 = 16 / esize;  // elements per 16 bytes
-  const int s = (hop + per16 - 1) / per16;
-  return (s | 1) * per16;
+__host__ __device__ constexpr int in_row_stride_x2_c(int hop, int esize) {
+  return ((((hop + 16 / esize - 1) / (16 / esize)) | 1) * (16 / esize));
 }
+__host__ __device__ inline int in_row_stride_x2(int hop, int esize) { return in_row_stride_x2_c(hop, esize); }
 
 // Layout of the two-frames-per-thread kernel (32-frame tiles): its tables
-// (copied once per CTA from the X2Tables block), two input tiles (double
-// buffering) and the exchange buffer.
+// (copied once per CTA from the X2Tables block) and the exchange buffer. The
+// power tile occupies the lower half of the exchange buffer after pass 2, and
+// the next tile's samples are staged into the upper half meanwhile, so a CTA
+// needs no separate input buffer (when a tile fits there; otherwise one is
+// appended).
 struct SmemLayoutX2 {
-  size_t bars, p1, tw_half, tw_full, chunks, mel_w, in_tile, in_tile_bytes, xbuf, total;
+  size_t bars, p1, tw_half, tw_full, chunks, mel_w, xbuf, in_tile, in_tile_bytes, total;
 };
 
 // n_chunks: mel chunks (int4 x 2 each); n_w: padded weight pairs
@@ -124,15 +126,22 @@ __host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n
   const int M = n_fft / 2;
   SmemLayoutX2 L;
   size_t o = 0;
-  L.bars = o;      o = align16(o + 2 * sizeof(unsigned long long));  // one mbarrier per input buffer
+  L.bars = o;      o = align16(o + 2 * sizeof(unsigned long long));
   L.p1 = o;        o = align16(o + sizeof(float4) * M);
   L.tw_half = o;   o = align16(o + sizeof(float4) * M);
   L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));
   L.chunks = o;    o = align16(o + sizeof(int4) * 2 * (n_chunks > 0 ? n_chunks : 1));
   L.mel_w = o;     o = align16(o + sizeof(float2) * (n_w > 0 ? n_w : 2));
+  const size_t xq_bytes = sizeof(float4) * 16 * (size_t)(M + 1);
+  const size_t half = xq_bytes / 2;  // = the power tile, (M + 1) bins x 16 lanes x float2
+  L.xbuf = o;      o = align16(o + xq_bytes);
   L.in_tile_bytes = align16((size_t)in_esize * in_rows(n_fft, hop, 32) * in_row_stride_x2(hop, in_esize));
-  L.in_tile = o;   o += 2 * L.in_tile_bytes;
-  L.xbuf = o;      o = align16(o + sizeof(float4) * 16 * (size_t)(M + 1));
+  if (L.in_tile_bytes <= xq_bytes - align16(half)) {
+    L.in_tile = L.xbuf + align16(half);
+  } else {
+    L.in_tile = o;
+    o += L.in_tile_bytes;
+  }
   L.total = o;
   return L;
 }
@@ -146,8 +155,10 @@ struct Variant {
   int in_buffers;       // 2: the next tile's input lands while this one computes
   int kind;             // 0: one frame per thread; 1: two frames per thread (packed)
   const void* fn;       // __global__ void(KernelParams)
+  int hop;              // > 0: compiled for this hop only; 0: any hop
 };
 
-const Variant* find_variant(int n_fft);
+// the kernel for (n_fft, hop): a hop-specialised build if there is one
+const Variant* find_variant(int n_fft, int hop);
 
 }  // namespace fm

@@ -465,5 +465,5 @@ __global__ void __launch_bounds__(P* G) mel_kernel(const KernelParams prm) {
 #define FM_DEFINE_VARIANT(NAME, N, P, Q, G, NBUF)                                                       \
   namespace fm {                                                                                        \
   template __global__ void mel_kernel<N, P, Q, G, NBUF>(const KernelParams);                          \
-  extern const Variant NAME = {N, P, Q, G, P * G, NBUF, 0, (const void*)&mel_kernel<N, P, Q, G, NBUF>}; \
+  extern const Variant NAME = {N, P, Q, G, P * G, NBUF, 0, (const void*)&mel_kernel<N, P, Q, G, NBUF>, 0}; \
   }

@@ -4,10 +4,14 @@
 // Same path and same four-step real FFT as fm_kernel.cuh, but a tile holds 32
 // frames and thread (role, g), g < 16, carries frames g and g + 16 through
 // every phase as packed pairs (see fm_fft2.cuh):
-//   staging : raw samples as rows of `hop`, double-buffered so the next tile
-//             lands while this one computes: TMA bulk copies (one per row,
-//             issued by warp 0, completing on an mbarrier) for interior tiles
-//             with 16-byte aligned rows, cp.async element copies otherwise;
+//   staging : raw samples as rows of `hop` in the upper half of the exchange
+//             buffer, which is free from the end of pass 2 (the power tile
+//             uses the lower half) to the start of the next pass 1: the next
+//             tile lands during the split and the mel projection. TMA bulk
+//             copies (one per row, issued by warp 0, completing on an
+//             mbarrier) for interior tiles with 16-byte aligned rows,
+//             cp.async element copies otherwise. Small shared memory per CTA
+//             (no separate input buffers) fits three CTAs per SM;
 //   tables  : window/offset, twiddles and filters are copied once per CTA
 //             into shared memory and read as broadcasts;
 //   pass 1  : two LDS.64 pair loads per step, the window multiply scatters
@@ -28,21 +32,48 @@ namespace fm {
 constexpr int kX2Lanes = 16;   // lanes per role
 constexpr int kX2Frames = 32;  // frames per tile
 
-template <int P, int Q, typename Raw>
-__device__ __forceinline__ void pass1_x2(const Raw* __restrict__ base_a, int S, const float4* __restrict__ s_p1,
-                                         const float4* __restrict__ s_twh4, float4* xq_row, int p) {
-  const Raw* base_b = base_a + kX2Lanes * S;
-  cx2 z[Q];
+// Pass 1, load half: the windowed pairs z[q] = (y[2n], y[2n+1]) / 2 with
+// n = p + P q, for frames g and g + 16 (frame base pointers base_a and
+// base_a + 16 rows). HOP > 0: the hop is a compile-time multiple of 2P, so the
+// tile offset of the pair is (2Pq / HOP) rows + (2Pq mod HOP) + 2p, a
+// compile-time constant plus 2p, and the loads need no address math.
+template <int P, int Q, int HOP, typename Raw>
+__device__ __forceinline__ void pass1_load_x2(const Raw* __restrict__ base_a, int S, const float4* __restrict__ s_p1,
+                                              int p, cx2 (&z)[Q]) {
   const float4* tab = s_p1 + p * Q;
+  if constexpr (HOP > 0) {
+    static_assert(HOP % (2 * P) == 0, "compile-time hop must be a multiple of 2P");
+    constexpr int SC = in_row_stride_x2_c(HOP, (int)sizeof(Raw));
+    const Raw* base = base_a + 2 * p;
 #pragma unroll
-  for (int q = 0; q < Q; ++q) {
-    const float4 e = tab[q];
-    const int off = __float_as_int(e.z);
-    const float2 va = load_pair(base_a + off);
-    const float2 vb = load_pair(base_b + off);
-    z[q].re = make_float2(va.x * e.x, vb.x * e.x);
-    z[q].im = make_float2(va.y * e.y, vb.y * e.y);
+    for (int q = 0; q < Q; ++q) {
+      const float2 w = *reinterpret_cast<const float2*>(tab + q);
+      const int off = (2 * P * q / HOP) * SC + (2 * P * q) % HOP;
+      const float2 va = load_pair(base + off);
+      const float2 vb = load_pair(base + off + kX2Lanes * SC);
+      z[q].re = make_float2(va.x * w.x, vb.x * w.x);
+      z[q].im = make_float2(va.y * w.y, vb.y * w.y);
+    }
+  } else {
+    const Raw* base_b = base_a + kX2Lanes * S;
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const float4 e = tab[q];
+      const int off = __float_as_int(e.z);
+      const float2 va = load_pair(base_a + off);
+      const float2 vb = load_pair(base_b + off);
+      z[q].re = make_float2(va.x * e.x, vb.x * e.x);
+      z[q].im = make_float2(va.y * e.y, vb.y * e.y);
+    }
   }
+}
+
+// Pass 1, compute half: Q-point DFT, four-step twiddle W_M^{p k2}, and one
+// 16-byte store {re_a, re_b, im_a, im_b} per output into row g of the
+// exchange buffer at [k2 * P + p].
+template <int P, int Q>
+__device__ __forceinline__ void pass1_finish_x2(cx2 (&z)[Q], const float4* __restrict__ s_twh4, float4* xq_row,
+                                                int p) {
   dft<Q>(z);
   xq_row[p] = make_float4(z[0].re.x, z[0].re.y, z[0].im.x, z[0].im.y);
 #pragma unroll
@@ -77,24 +108,30 @@ __device__ __forceinline__ void split_pair_x2(cx2 zk, cx2 zm, float4 w, float pw
   out_mk = power2<MODE>(sub2(s.re, v.im), add2(s.im, v.re), pw);
 }
 
-// Pass 2 and split for Q = 2P; power pairs go to pw_col[k * 16] (float2).
-template <int N, int P, int Q, int MODE>
-__device__ __forceinline__ void pass2_split_x2(const float4* xq_row, float2* pw_col, const float4* __restrict__ s_twf4,
-                                               int t, float pw) {
-  constexpr int M = N / 2;
+// Pass 2 for Q = 2P: role t >= 1 holds k2 = t and Q - t, role 0 holds k2 = 0
+// and Q/2; P-point DFTs over p give a[k1] = Z[kA + Q k1], b[k1] = Z[kB + Q k1].
+template <int P, int Q>
+__device__ __forceinline__ void pass2_x2(const float4* xq_row, int t, cx2 (&a)[P], cx2 (&b)[P]) {
   static_assert(Q == 2 * P && P % 2 == 0, "paired split needs Q = 2P with P even");
   const int kA = t;
   const int kB = (t == 0) ? Q / 2 : Q - t;
-  cx2 a[P], b[P];
 #pragma unroll
   for (int p = 0; p < P; ++p) {
     a[p] = load_cx2(xq_row + kA * P + p);
     b[p] = load_cx2(xq_row + kB * P + p);
   }
-  dft<P>(a);  // a[k1] = Z[kA + Q k1]
-  dft<P>(b);  // b[k1] = Z[kB + Q k1]
-  __syncthreads();  // every exchange read is done: the power tile may overwrite it
+  dft<P>(a);
+  dft<P>(b);
+}
+
+// Real-FFT split of pass 2's outputs: both members of every pair (k, M - k)
+// are in this thread's registers; power pairs go to pw_col[k * 16] (float2).
+template <int N, int P, int Q, int MODE>
+__device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], float2* pw_col,
+                                         const float4* __restrict__ s_twf4, int t, float pw) {
+  constexpr int M = N / 2;
   if (t != 0) {
+    // Z[t + Q k1] pairs with Z[(Q - t) + Q (P - 1 - k1)]
 #pragma unroll
     for (int k1 = 0; k1 < P; ++k1) {
       const int k = t + Q * k1;
@@ -104,6 +141,8 @@ __device__ __forceinline__ void pass2_split_x2(const float4* xq_row, float2* pw_
       pw_col[(M - k) * kX2Lanes] = hi;
     }
   } else {
+    // k = Q k1 pairs with Q (P - k1) (k1 = 0 gives X[0] and X[M]); k = Q/2 + Q k1
+    // pairs with Q/2 + Q (P - 1 - k1)
 #pragma unroll
     for (int k1 = 0; k1 <= P / 2; ++k1) {
       const int k = Q * k1;
@@ -164,7 +203,7 @@ __device__ __forceinline__ void mel_project_x2(const float2* s_pw2, const int4* 
   }
 }
 
-template <int N, int P, int Q, typename Raw>
+template <int N, int P, int Q, int HOP, typename Raw>
 __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay) {
   constexpr int M = N / 2;
   constexpr int THREADS = P * kX2Lanes;
@@ -181,13 +220,12 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = tid % kX2Lanes, role = tid / kX2Lanes;
   const int esize = (int)sizeof(Raw);
-  const int hop = prm.hop, S = in_row_stride_x2(hop, esize), rows = in_rows(N, hop, kX2Frames);
+  const int hop = HOP > 0 ? HOP : prm.hop, S = in_row_stride_x2(hop, esize), rows = in_rows(N, hop, kX2Frames);
   const Raw* in = static_cast<const Raw*>(prm.in);
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
   const int s_begin = __ldg(&prm.x2->warp_begin[warp]), s_end = __ldg(&prm.x2->warp_begin[warp + 1]);
   unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + lay.bars);
-  auto in_buf = [&](int i) { return reinterpret_cast<Raw*>(smem + lay.in_tile + (size_t)i * lay.in_tile_bytes); };
   // Where a tile lives: signal b, tile index tt within it, signal index of
   // tile position 0, and whether it is interior with 16-byte aligned rows
   // (then TMA bulk copies stage it). Computed once per tile and carried.
@@ -205,64 +243,68 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
              (reinterpret_cast<uintptr_t>(src + pl.gstart) & 15) == 0;
     return pl;
   };
-  // Stage a tile into buffer `buf`: TMA row copies issued by warp 0 (one row
-  // per lane), or cp.async element copies by all threads at the signal edges.
-  // A buffer last filled by cp.async gets a proxy fence before TMA refills it.
-  unsigned filled_by_cp = 0u;  // bit b: buffer b was last filled by cp.async
-  auto stage = [&](const Place& pl, int buf) {
+  // Stage a tile into the input area: TMA row copies issued by warp 0 (one row
+  // per lane) completing on the mbarrier, or cp.async element copies by all
+  // threads at the signal edges. The area was last written through the
+  // generic proxy (exchange stores), hence the proxy fence before TMA.
+  Raw* s_in = reinterpret_cast<Raw*>(smem + lay.in_tile);
+  auto stage = [&](const Place& pl) {
     const Raw* src = in + pl.b * T;
     if (pl.tma) {
       if (warp == 0) {
         if (lane == 0) {
-          if ((filled_by_cp >> buf) & 1u) fence_proxy_async();
-          mbar_arrive_expect_tx(&bars[buf], (unsigned)(rows * hop * esize));
+          fence_proxy_async();
+          mbar_arrive_expect_tx(&bars[0], (unsigned)(rows * hop * esize));
         }
         __syncwarp();
         for (int r = lane; r < rows; r += 32)
-          tma_load_1d(in_buf(buf) + r * S, src + pl.gstart + (long long)r * hop, (unsigned)(hop * esize), &bars[buf]);
+          tma_load_1d(s_in + r * S, src + pl.gstart + (long long)r * hop, (unsigned)(hop * esize), &bars[0]);
       }
     } else {
-      stage_tile<Raw, NWARPS>(src, T, pl.gstart, rows, hop, S, in_buf(buf), warp, lane);
+      stage_tile<Raw, NWARPS>(src, T, pl.gstart, rows, hop, S, s_in, warp, lane);
     }
-    filled_by_cp = (filled_by_cp & ~(1u << buf)) | ((pl.tma ? 0u : 1u) << buf);
     cp_async_commit();
   };
   if (tid == 0) {
     mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
     fence_mbar_init();
   }
-  __syncthreads();  // the barriers exist before anyone polls them
-  unsigned phase = 0u;  // bit b: parity of buffer b's next mbarrier phase
+  __syncthreads();  // the barrier exists before anyone polls it
+  unsigned phase = 0u;
 
   long long tile = blockIdx.x;
-  int buf = 0;
   Place cur = locate(tile);
-  if (tile < prm.total_tiles) stage(cur, 0);
-  for (; tile < prm.total_tiles; tile += gridDim.x, buf ^= 1) {
+  if (tile < prm.total_tiles) stage(cur);
+  for (; tile < prm.total_tiles; tile += gridDim.x) {
     cp_async_wait_all();
     bool failed = false;
     if (cur.tma) {
-      failed = !mbar_wait_bounded(&bars[buf], (phase >> buf) & 1u, prm.err);
-      phase ^= 1u << buf;
+      failed = !mbar_wait_bounded(&bars[0], phase, prm.err);
+      phase ^= 1u;
     }
-    // this tile's samples are visible; the previous tile is fully done
+    // this tile's samples are visible; the previous tile's mel phase is done
     if (__syncthreads_or(failed)) return;  // a staging copy never arrived (error recorded)
+
+    float4* xq_row = s_xq + g * GS4;
+    cx2 z[Q];
+    pass1_load_x2<P, Q, HOP, Raw>(s_in + g * S, S, s_p1, role, z);
+    __syncthreads();  // samples are in registers: the exchange buffer (holding them) may be overwritten
+    pass1_finish_x2<P, Q>(z, s_twh4, xq_row, role);
+    __syncthreads();
+
+    cx2 za[P], zb[P];
+    pass2_x2<P, Q>(xq_row, role, za, zb);
+    __syncthreads();  // exchange reads done: power tile (lower half) and next tile (upper half) may land
     const long long next = tile + gridDim.x;
     Place nxt{};
     if (next < prm.total_tiles) {
       nxt = locate(next);
-      stage(nxt, buf ^ 1);  // lands while this tile computes
+      stage(nxt);  // lands during the split and the mel projection
     }
-
-    float4* xq_row = s_xq + g * GS4;
-    pass1_x2<P, Q, Raw>(in_buf(buf) + g * S, S, s_p1, s_twh4, xq_row, role);
-    __syncthreads();
-
     switch (prm.power_mode) {
-      case 0: pass2_split_x2<N, P, Q, 0>(xq_row, s_pw2 + g, s_twf4, role, prm.power); break;
-      case 1: pass2_split_x2<N, P, Q, 1>(xq_row, s_pw2 + g, s_twf4, role, prm.power); break;
-      default: pass2_split_x2<N, P, Q, 2>(xq_row, s_pw2 + g, s_twf4, role, prm.power); break;
+      case 0: split_x2<N, P, Q, 0>(za, zb, s_pw2 + g, s_twf4, role, prm.power); break;
+      case 1: split_x2<N, P, Q, 1>(za, zb, s_pw2 + g, s_twf4, role, prm.power); break;
+      default: split_x2<N, P, Q, 2>(za, zb, s_pw2 + g, s_twf4, role, prm.power); break;
     }
     __syncthreads();
 
@@ -281,8 +323,8 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   cp_async_wait_all();
 }
 
-template <int N, int P, int Q>
-__global__ void __launch_bounds__(P* kX2Lanes) mel_kernel_x2(const KernelParams prm) {
+template <int N, int P, int Q, int HOP>
+__global__ void __launch_bounds__(P* kX2Lanes, 3) mel_kernel_x2(const KernelParams prm) {
   constexpr int M = N / 2;
   constexpr int THREADS = P * kX2Lanes;
   static_assert(P * Q == M && Q == 2 * P && M <= kX2MaxM, "x2 kernel needs Q = 2P and M <= 200");
@@ -298,17 +340,18 @@ __global__ void __launch_bounds__(P* kX2Lanes) mel_kernel_x2(const KernelParams 
   copy_table_async(smem + lay.tw_full, t->tw_full, (int)sizeof(float4) * (M + 1), tid, THREADS);
   copy_table_async(smem + lay.chunks, t->chunk, (int)sizeof(int4) * 2 * prm.x2_chunks, tid, THREADS);
   copy_table_async(smem + lay.mel_w, t->mel_w, (int)sizeof(float2) * prm.x2_w, tid, THREADS);
-  if (prm.in_dtype == FM_F32) run_tiles_x2<N, P, Q, float>(prm, smem, lay);
-  else if (prm.in_dtype == FM_I16) run_tiles_x2<N, P, Q, short>(prm, smem, lay);
-  else run_tiles_x2<N, P, Q, __half>(prm, smem, lay);
+  if (prm.in_dtype == FM_F32) run_tiles_x2<N, P, Q, HOP, float>(prm, smem, lay);
+  else if (prm.in_dtype == FM_I16) run_tiles_x2<N, P, Q, HOP, short>(prm, smem, lay);
+  else run_tiles_x2<N, P, Q, HOP, __half>(prm, smem, lay);
 }
 
 }  // namespace fm
 
-// Instantiate one two-frames-per-thread variant: FM_DEFINE_VARIANT_X2(name, N, P, Q)
-#define FM_DEFINE_VARIANT_X2(NAME, N, P, Q)                                                   \
+// Instantiate one two-frames-per-thread variant:
+// FM_DEFINE_VARIANT_X2(name, N, P, Q, HOP) with HOP = 0 for any hop
+#define FM_DEFINE_VARIANT_X2(NAME, N, P, Q, HOP)                                              \
   namespace fm {                                                                              \
-  template __global__ void mel_kernel_x2<N, P, Q>(const KernelParams);                       \
-  extern const Variant NAME = {N, P, Q, kX2Frames, P * kX2Lanes, 1, 1,                         \
-                               (const void*)&mel_kernel_x2<N, P, Q>};                          \
+  template __global__ void mel_kernel_x2<N, P, Q, HOP>(const KernelParams);                  \
+  extern const Variant NAME = {N, P, Q, kX2Frames, P * kX2Lanes, 2, 1,                         \
+                               (const void*)&mel_kernel_x2<N, P, Q, HOP>, HOP};               \
   }
