@@ -367,8 +367,20 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
   prm.x2 = plan->x2;
   void* args[] = {&prm};
-  const cudaError_t e = cudaLaunchKernel(v->fn, dim3((unsigned)grid), dim3(v->threads), args, plan->smem,
-                                         reinterpret_cast<cudaStream_t>(stream));
+  // programmatic dependent launch: the kernel waits (griddepcontrol.wait) for
+  // the previous kernel in the stream before it reads d_in or writes d_out, so
+  // only set-up overlaps; a predecessor that did not opt in is waited for in full
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(v->threads);
+  cfg.dynamicSmemBytes = plan->smem;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, v->fn, args);
   return e == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 

@@ -93,6 +93,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, unsig
   return false;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start its
+// CTAs (as SM slots free up) and do its own set-up while this one runs; and,
+// before touching any caller buffer, wait until the previous kernel in the
+// stream has completed and its memory is visible. Both are no-ops when the
+// launch did not opt in.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // a pair of consecutive samples (2n, 2n+1) from the staged tile, as floats
 __device__ __forceinline__ float2 load_pair(const float* p) { return *reinterpret_cast<const float2*>(p); }
 __device__ __forceinline__ float2 load_pair(const short* p) {
@@ -444,6 +452,7 @@ __global__ void __launch_bounds__(P* G) mel_kernel(const KernelParams prm) {
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
   const SmemLayout lay = smem_layout(N, prm.hop, prm.n_mels, prm.nnz, G, esize, NBUF);
 
+  pdl_launch_dependents();
   // per-CTA constant tables, fetched once (the grid is persistent) in the same
   // cp.async group as the first tile, so one wait covers both
   const int tid = threadIdx.x;
@@ -452,6 +461,7 @@ __global__ void __launch_bounds__(P* G) mel_kernel(const KernelParams prm) {
   copy_table_async(smem + lay.tw_full, prm.tw_full, (int)sizeof(float2) * (M + 1) + ((M + 1) & 1) * 8, tid, THREADS);
   copy_table_async(smem + lay.mel, prm.mel, (int)sizeof(int4) * prm.n_mels, tid, THREADS);
   copy_table_async(smem + lay.mel_w, prm.mel_w, (int)align16(sizeof(float) * (prm.nnz > 0 ? prm.nnz : 1)), tid, THREADS);
+  pdl_wait();  // caller buffers only after the previous kernel in the stream is done
   // (the first barrier inside run_tiles publishes the tables)
 
   if (prm.in_dtype == FM_F32) run_tiles<N, P, Q, G, NBUF, float>(prm, smem, lay);

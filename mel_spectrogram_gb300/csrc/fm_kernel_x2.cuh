@@ -270,6 +270,7 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     fence_mbar_init();
   }
   __syncthreads();  // the barrier exists before anyone polls it
+  pdl_wait();       // caller buffers only after the previous kernel in the stream is done
   unsigned phase = 0u;
 
   long long tile = blockIdx.x;
@@ -279,7 +280,9 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     cp_async_wait_all();
     bool failed = false;
     if (cur.tma) {
-      failed = !mbar_wait_bounded(&bars[0], phase, prm.err);
+      // one thread waits for the copies; the barrier below then orders them
+      // for the whole CTA while the other warps sleep instead of polling
+      if (tid == 0) failed = !mbar_wait_bounded(&bars[0], phase, prm.err);
       phase ^= 1u;
     }
     // this tile's samples are visible; the previous tile's mel phase is done
@@ -332,6 +335,7 @@ __global__ void __launch_bounds__(P* kX2Lanes, 3) mel_kernel_x2(const KernelPara
   extern __shared__ __align__(16) unsigned char smem[];
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
   const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, prm.x2_chunks, prm.x2_w, esize);
+  pdl_launch_dependents();
   // tables, fetched once per CTA in the first tile's cp.async group
   const int tid = threadIdx.x;
   const X2Tables* t = prm.x2;
