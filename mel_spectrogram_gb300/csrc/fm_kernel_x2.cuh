@@ -124,14 +124,21 @@ __device__ __forceinline__ void pass2_x2(const float4* xq_row, int t, cx2 (&a)[P
   dft<P>(b);
 }
 
+__device__ __forceinline__ cx2 sel(bool c, const cx2& a, const cx2& b) { return c ? a : b; }
+
 // Real-FFT split of pass 2's outputs: both members of every pair (k, M - k)
 // are in this thread's registers; power pairs go to pw_col[k * 16] (float2).
+//   role t >= 1: pairs (a[j], b[P-1-j]) at k = t + Q j, j < P;
+//   role 0:      pairs (a[j], a[(P-j) % P]) at k = Q j, j <= P/2 (j = 0 gives
+//                X[0] and X[M]), and (b[i], b[P-1-i]) at k = Q/2 + Q i, i < P/2.
+// The warp holding role 0 (with role 1 beside it) runs both as one stream of
+// P + 1 slots with the operands chosen by selects, so it does not execute two
+// divergent paths while the other warps wait at the next barrier.
 template <int N, int P, int Q, int MODE>
 __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], float2* pw_col,
-                                         const float4* __restrict__ s_twf4, int t, float pw) {
+                                         const float4* __restrict__ s_twf4, int t, float pw, bool merged) {
   constexpr int M = N / 2;
-  if (t != 0) {
-    // Z[t + Q k1] pairs with Z[(Q - t) + Q (P - 1 - k1)]
+  if (!merged) {
 #pragma unroll
     for (int k1 = 0; k1 < P; ++k1) {
       const int k = t + Q * k1;
@@ -140,22 +147,29 @@ __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], f
       pw_col[k * kX2Lanes] = lo;
       pw_col[(M - k) * kX2Lanes] = hi;
     }
-  } else {
-    // k = Q k1 pairs with Q (P - k1) (k1 = 0 gives X[0] and X[M]); k = Q/2 + Q k1
-    // pairs with Q/2 + Q (P - 1 - k1)
+    return;
+  }
+  const bool r0 = (t == 0);
 #pragma unroll
-    for (int k1 = 0; k1 <= P / 2; ++k1) {
-      const int k = Q * k1;
-      float2 lo, hi;
-      split_pair_x2<MODE>(a[k1], a[(P - k1) % P], s_twf4[k], pw, lo, hi);
-      pw_col[k * kX2Lanes] = lo;
-      pw_col[(M - k) * kX2Lanes] = hi;
+  for (int j = 0; j <= P; ++j) {
+    cx2 u, v;
+    int k;
+    if (j <= P / 2) {
+      u = a[j];
+      v = sel(r0, a[(P - j) % P], b[P - 1 - j]);
+      k = t + Q * j;
+    } else if (j < P) {
+      u = sel(r0, b[j - P / 2 - 1], a[j]);
+      v = sel(r0, b[3 * P / 2 - j], b[P - 1 - j]);
+      k = r0 ? Q / 2 + Q * (j - P / 2 - 1) : t + Q * j;
+    } else {  // the one extra pair of role 0
+      u = b[P / 2 - 1];
+      v = b[P / 2];
+      k = Q / 2 + Q * (P / 2 - 1);
     }
-#pragma unroll
-    for (int k1 = 0; k1 < P / 2; ++k1) {
-      const int k = Q / 2 + Q * k1;
+    if (j < P || r0) {
       float2 lo, hi;
-      split_pair_x2<MODE>(b[k1], b[P - 1 - k1], s_twf4[k], pw, lo, hi);
+      split_pair_x2<MODE>(u, v, s_twf4[k], pw, lo, hi);
       pw_col[k * kX2Lanes] = lo;
       pw_col[(M - k) * kX2Lanes] = hi;
     }
@@ -243,21 +257,21 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
              (reinterpret_cast<uintptr_t>(src + pl.gstart) & 15) == 0;
     return pl;
   };
-  // Stage a tile into the input area: TMA row copies issued by warp 0 (one row
-  // per lane) completing on the mbarrier, or cp.async element copies by all
-  // threads at the signal edges. The area was last written through the
-  // generic proxy (exchange stores), hence the proxy fence before TMA.
+  // Stage a tile into the input area: TMA row copies issued by one lane of
+  // every warp (rows dealt round robin) completing on the mbarrier, or
+  // cp.async element copies by all threads at the signal edges. The area was
+  // last written through the generic proxy (exchange stores), hence the proxy
+  // fence before each issuing lane's first copy.
   Raw* s_in = reinterpret_cast<Raw*>(smem + lay.in_tile);
   auto stage = [&](const Place& pl) {
     const Raw* src = in + pl.b * T;
     if (pl.tma) {
-      if (warp == 0) {
-        if (lane == 0) {
-          fence_proxy_async();
-          mbar_arrive_expect_tx(&bars[0], (unsigned)(rows * hop * esize));
-        }
-        __syncwarp();
-        for (int r = lane; r < rows; r += 32)
+      // The barrier's single arrival carries the byte count, so its phase
+      // cannot complete before it even if some copies land first.
+      if (tid == 0) mbar_arrive_expect_tx(&bars[0], (unsigned)(rows * hop * esize));
+      if (lane == 0) {
+        fence_proxy_async();
+        for (int r = warp; r < rows; r += NWARPS)
           tma_load_1d(s_in + r * S, src + pl.gstart + (long long)r * hop, (unsigned)(hop * esize), &bars[0]);
       }
     } else {
@@ -304,10 +318,11 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
       nxt = locate(next);
       stage(nxt);  // lands during the split and the mel projection
     }
+    const bool merged = role < 2;  // the warp that holds role 0 (and role 1)
     switch (prm.power_mode) {
-      case 0: split_x2<N, P, Q, 0>(za, zb, s_pw2 + g, s_twf4, role, prm.power); break;
-      case 1: split_x2<N, P, Q, 1>(za, zb, s_pw2 + g, s_twf4, role, prm.power); break;
-      default: split_x2<N, P, Q, 2>(za, zb, s_pw2 + g, s_twf4, role, prm.power); break;
+      case 0: split_x2<N, P, Q, 0>(za, zb, s_pw2 + g, s_twf4, role, prm.power, merged); break;
+      case 1: split_x2<N, P, Q, 1>(za, zb, s_pw2 + g, s_twf4, role, prm.power, merged); break;
+      default: split_x2<N, P, Q, 2>(za, zb, s_pw2 + g, s_twf4, role, prm.power, merged); break;
     }
     __syncthreads();
 
