@@ -47,84 +47,77 @@ struct fm_plan {
   float2* mel_w2;
   unsigned* err;
   fm::X2Tables* x2;  // device tables of the two-frames-per-thread kernel (inside dmem)
-  int x2_chunks, x2_w;  // its mel chunk count and padded weight-pair count
+  int x2_slots;         // its mel chunk slots
 };
 
 namespace {
 
 int dtype_size(int dt) { return dt == FM_F32 ? 4 : 2; }
 
-// Mel schedule of the two-frames-per-thread kernel. Filters 2i and 2i+1 form
-// a step, both padded to one even length L >= 2 (zero weights; a run that
-// would pass bin M is shifted left), cut into L/2 two-bin chunks. Steps are
-// dealt to warps to balance their chunk counts (largest first onto the least
-// loaded warp) and each warp's chunk list is padded with no-op chunks to a
-// multiple of the kernel's unroll.
+// Mel schedule of the two-frames-per-thread kernel: four chunk streams per
+// warp (one per quarter-warp). Each filter is padded to an even length
+// L >= 2 (zero weights; a run that would pass bin M is shifted left) and cut
+// into L/2 two-bin chunks; filters are dealt to streams to balance their
+// chunk counts (largest first onto the least loaded stream), and the four
+// streams of a warp are padded with no-op chunks to one length, a multiple of
+// the kernel's unroll. Layout as in X2Tables.
 struct X2Schedule {
   std::vector<int> warp_begin;
-  std::vector<int4> chunks;  // 2 per chunk (one per half-warp)
-  std::vector<float2> w;
+  std::vector<int2> desc;   // 4 per slot
+  std::vector<float4> w4;   // 4 per slot
 };
 
 X2Schedule build_x2_schedule(int M, int n_mels, int n_warps, const std::vector<int>& ms, const std::vector<int>& ml,
                              const std::vector<int>& mo, const std::vector<float>& mw) {
-  struct Step { int m[2]; int L; };
-  std::vector<Step> raw;
-  for (int i = 0; 2 * i < n_mels; ++i) {
-    Step st;
-    st.m[0] = 2 * i;
-    st.m[1] = 2 * i + 1 < n_mels ? 2 * i + 1 : -1;
-    int L = ml[st.m[0]];
-    if (st.m[1] >= 0 && ml[st.m[1]] > L) L = ml[st.m[1]];
-    L += L & 1;
-    st.L = L < 2 ? 2 : L;
-    raw.push_back(st);
-  }
-  std::vector<int> order(raw.size());
-  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
-  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return raw[a].L > raw[b].L; });
-  std::vector<std::vector<int>> per(n_warps);
-  std::vector<int> load(n_warps, 0);
-  for (int i : order) {
-    int wmin = 0;
-    for (int k = 1; k < n_warps; ++k)
-      if (load[k] < load[wmin]) wmin = k;
-    per[wmin].push_back(i);
-    load[wmin] += raw[i].L / 2;
-  }
-  X2Schedule S;
-  S.w.assign(2, make_float2(0.0f, 0.0f));  // a zero weight pair for the no-op chunks
-  S.warp_begin.push_back(0);
-  for (int k = 0; k < n_warps; ++k) {
-    for (int i : per[k]) {
-      const Step& st = raw[i];
-      int start[2], woff[2];
-      for (int h = 0; h < 2; ++h) {
-        const int m = st.m[h];
-        start[h] = m >= 0 ? ms[m] : 0;
-        int lead = 0;
-        if (start[h] + st.L > M + 1) {
-          lead = start[h] + st.L - (M + 1);
-          start[h] -= lead;
-        }
-        woff[h] = (int)S.w.size();
-        for (int j = 0; j < st.L; ++j) {
-          const int k2 = j - lead;
-          const float v = (m >= 0 && k2 >= 0 && k2 < ml[m]) ? mw[mo[m] + k2] : 0.0f;
-          S.w.push_back(make_float2(v, v));
-        }
-      }
-      for (int c = 0; c < st.L / 2; ++c) {
-        const int flags = (c == 0 ? fm::kChunkFirst : 0) | (c == st.L / 2 - 1 ? fm::kChunkLast : 0);
-        for (int h = 0; h < 2; ++h)
-          S.chunks.push_back(make_int4((start[h] + 2 * c) * 16 * (int)sizeof(float2),
-                                       (woff[h] + 2 * c) * (int)sizeof(float2), st.m[h] >= 0 ? st.m[h] : 0,
-                                       st.m[h] >= 0 ? flags : (flags & fm::kChunkFirst)));
-      }
+  struct Chunk { int2 d; float4 w; };
+  auto chunks_of = [&](int m) {
+    int L = ml[m] + (ml[m] & 1);
+    L = L < 2 ? 2 : L;
+    int start = ms[m], lead = 0;
+    if (start + L > M + 1) {
+      lead = start + L - (M + 1);
+      start -= lead;
     }
-    while ((S.chunks.size() / 2) % fm::kX2Unroll != 0)
-      for (int h = 0; h < 2; ++h) S.chunks.push_back(make_int4(0, 0, 0, 0));
-    S.warp_begin.push_back((int)(S.chunks.size() / 2));
+    auto weight = [&](int j) {
+      const int k2 = j - lead;
+      return (k2 >= 0 && k2 < ml[m]) ? mw[mo[m] + k2] : 0.0f;
+    };
+    std::vector<Chunk> out;
+    for (int c = 0; c < L / 2; ++c) {
+      const float w0 = weight(2 * c), w1 = weight(2 * c + 1);
+      out.push_back({make_int2((start + 2 * c) * 16 * (int)sizeof(float2), c == L / 2 - 1 ? m : -1),
+                     make_float4(w0, w0, w1, w1)});
+    }
+    return out;
+  };
+  const int n_streams = 4 * n_warps;
+  std::vector<int> order(n_mels);
+  for (int m = 0; m < n_mels; ++m) order[m] = m;
+  auto n_chunks = [&](int m) { return ml[m] < 2 ? 1 : (ml[m] + 1) / 2; };
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return n_chunks(a) > n_chunks(b); });
+  std::vector<std::vector<Chunk>> stream(n_streams);
+  for (int m : order) {
+    int s = 0;
+    for (int k = 1; k < n_streams; ++k)
+      if (stream[k].size() < stream[s].size()) s = k;
+    const std::vector<Chunk> c = chunks_of(m);
+    stream[s].insert(stream[s].end(), c.begin(), c.end());
+  }
+  const Chunk noop = {make_int2(0, -1), make_float4(0.0f, 0.0f, 0.0f, 0.0f)};
+  X2Schedule S;
+  S.warp_begin.push_back(0);
+  for (int w = 0; w < n_warps; ++w) {
+    size_t len = 0;
+    for (int h = 0; h < 4; ++h) len = std::max(len, stream[4 * w + h].size());
+    len = (len + fm::kX2Unroll - 1) / fm::kX2Unroll * fm::kX2Unroll;
+    for (size_t c = 0; c < len; ++c)
+      for (int h = 0; h < 4; ++h) {
+        const std::vector<Chunk>& st = stream[4 * w + h];
+        const Chunk& k = c < st.size() ? st[c] : noop;
+        S.desc.push_back(k.d);
+        S.w4.push_back(k.w);
+      }
+    S.warp_begin.push_back(S.warp_begin.back() + (int)len);
   }
   return S;
 }
@@ -170,7 +163,7 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   const int nnz = (int)mw.size();
   X2Schedule x2s;
   if (var->kind == 1) x2s = build_x2_schedule(n_fft / 2, n_mels, var->threads / 32, ms, ml, mo, mw);
-  const int x2_chunks = (int)(x2s.chunks.size() / 2), x2_w = (int)x2s.w.size();
+  const int x2_slots = var->kind == 1 ? x2s.warp_begin.back() : 0;
 
   int dev = 0;
   cudaDeviceProp prop;
@@ -178,9 +171,9 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
   const int in_esize = in_dtype == FM_F32 ? 4 : 2;
   const size_t smem_total =
-      var->kind == 1 ? fm::smem_layout_x2(n_fft, hop, x2_chunks, x2_w, in_esize).total
+      var->kind == 1 ? fm::smem_layout_x2(n_fft, hop, x2_slots, in_esize).total
                      : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
-  if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_chunks > fm::kX2MaxChunks || x2_w > fm::kX2MaxW ||
+  if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_slots > fm::kX2MaxSlots ||
                          var->threads / 32 > fm::kX2MaxWarps))
     return FM_ERR_UNSUPPORTED;
   if (smem_total > (size_t)prop.sharedMemPerBlockOptin) return FM_ERR_UNSUPPORTED;
@@ -212,8 +205,7 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   p->power_mode = power == 2.0 ? 0 : power == 1.0 ? 1 : 2;
   p->var = var;
   p->nnz = nnz;
-  p->x2_chunks = x2_chunks;
-  p->x2_w = x2_w;
+  p->x2_slots = x2_slots;
   p->smem = smem_total;
   p->blocks_per_sm = bps;
   p->num_sms = prop.multiProcessorCount;
@@ -264,8 +256,8 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
     std::memcpy(t->tw_half, twh4.data(), sizeof(float4) * M);
     std::memcpy(t->tw_full, twf4.data(), sizeof(float4) * (M + 1));
     for (size_t i = 0; i < x2s.warp_begin.size(); ++i) t->warp_begin[i] = x2s.warp_begin[i];
-    std::memcpy(t->chunk, x2s.chunks.data(), sizeof(int4) * x2s.chunks.size());
-    if (x2_w > 0) std::memcpy(t->mel_w, x2s.w.data(), sizeof(float2) * x2_w);
+    std::memcpy(t->desc, x2s.desc.data(), sizeof(int2) * x2s.desc.size());
+    std::memcpy(t->w4, x2s.w4.data(), sizeof(float4) * x2s.w4.size());
   }
   std::memcpy(blob.data() + o_p1, p1.data(), sizeof(float4) * M);
   std::memcpy(blob.data() + o_twh, twh.data(), sizeof(float2) * M);
@@ -348,8 +340,7 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.out_dtype = plan->out_dtype;
   prm.n_mels = plan->n_mels;
   prm.nnz = plan->nnz;
-  prm.x2_chunks = plan->x2_chunks;
-  prm.x2_w = plan->x2_w;
+  prm.x2_slots = plan->x2_slots;
   prm.power_mode = plan->power_mode;
   prm.power = (float)plan->power;
   prm.tiles_per_signal = (prm.n_frames + v->frames_per_tile - 1) / v->frames_per_tile;

@@ -39,7 +39,7 @@ struct KernelParams {
   const float4* tw_full4;
   const float2* mel_w2;
   const struct X2Tables* x2;  // two-frames-per-thread kernel only
-  int x2_chunks, x2_w;        // its mel chunk count and padded weight-pair count
+  int x2_slots;               // its mel chunk slots (X2Tables::desc rows in use)
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
 };
 
@@ -81,25 +81,26 @@ __host__ __device__ inline SmemLayout smem_layout(int n_fft, int hop, int n_mels
 // every bin lies in at most two triangles, so nnz <= 2 (M + 1).
 constexpr int kX2MaxM = 200;
 constexpr int kX2MaxMels = 256;
-constexpr int kX2MaxW = 2 * (kX2MaxM + 1) + 4 * kX2MaxMels + 2;  // padded weight pairs
 constexpr int kX2MaxWarps = 16;
-constexpr int kX2Unroll = 4;  // chunks per unrolled mel iteration
-constexpr int kX2MaxChunks = kX2MaxW / 2 + kX2Unroll * kX2MaxWarps;
-enum { kChunkFirst = 1, kChunkLast = 2 };
+constexpr int kX2Unroll = 4;    // chunks per unrolled mel iteration
+constexpr int kX2MaxSlots = 1024;  // mel chunk slots (4 chunks each) over all warps
 struct X2Tables {
   float4 p1[kX2MaxM];        // as KernelParams::p1
   float4 tw_half[kX2MaxM];   // {c, c, d, d}, W_M^j = c + i d
   float4 tw_full[kX2MaxM + 1];
-  // Mel work as a stream of chunks. Filters 2i and 2i+1 (one per half-warp)
-  // are padded to one even length L >= 2 and cut into L/2 chunks of two
-  // bins; each warp runs its chunks [warp_begin[w], warp_begin[w + 1]), a
-  // multiple of kX2Unroll long (padded with no-op chunks). chunk[c][h] =
-  // {byte offset of the chunk's first bin in a lane's power column
-  // (bin * 128), byte offset of its two weight pairs (16-byte aligned),
-  // filter index, flags (kChunkFirst: start a sum, kChunkLast: store it)}.
+  // Mel work as four chunk streams per warp, one per quarter-warp. Every
+  // filter is padded to an even length L >= 2 (zero weights; a run that would
+  // pass bin M is shifted left) and cut into L/2 chunks of two bins; filters
+  // are dealt to streams to balance their chunk counts, and the four streams
+  // of warp w share slots [warp_begin[w], warp_begin[w + 1]), a multiple of
+  // kX2Unroll long (padded with no-op chunks). Slot s, quarter h:
+  //   desc[s][h] = {byte offset of the chunk's first bin row in the power
+  //                 tile (bin * 128), filter index if the chunk ends its
+  //                 filter (store and restart the sum), else -1};
+  //   w4[s][h]   = {w0, w0, w1, w1}, the weights of the two bins.
   int warp_begin[kX2MaxWarps + 1];
-  int4 chunk[kX2MaxChunks][2];
-  float2 mel_w[kX2MaxW];     // {w, w}; zeros where a filter was padded
+  int2 desc[kX2MaxSlots][4];
+  float4 w4[kX2MaxSlots][4];
 };
 
 // Row stride (elements) of the packed kernel's staged tile: each row starts
@@ -118,20 +119,21 @@ __host__ __device__ inline int in_row_stride_x2(int hop, int esize) { return in_
 // needs no separate input buffer (when a tile fits there; otherwise one is
 // appended).
 struct SmemLayoutX2 {
-  size_t bars, p1, tw_half, tw_full, chunks, mel_w, xbuf, in_tile, in_tile_bytes, total;
+  size_t bars, p1, tw_half, tw_full, desc, w4, xbuf, in_tile, in_tile_bytes, total;
 };
 
-// n_chunks: mel chunks (int4 x 2 each); n_w: padded weight pairs
-__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n_chunks, int n_w, int in_esize) {
+// n_slots: mel chunk slots (four chunks each)
+__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n_slots, int in_esize) {
   const int M = n_fft / 2;
+  const int ns = n_slots > 0 ? n_slots : 1;
   SmemLayoutX2 L;
   size_t o = 0;
   L.bars = o;      o = align16(o + 2 * sizeof(unsigned long long));
   L.p1 = o;        o = align16(o + sizeof(float4) * M);
   L.tw_half = o;   o = align16(o + sizeof(float4) * M);
   L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));
-  L.chunks = o;    o = align16(o + sizeof(int4) * 2 * (n_chunks > 0 ? n_chunks : 1));
-  L.mel_w = o;     o = align16(o + sizeof(float2) * (n_w > 0 ? n_w : 2));
+  L.desc = o;      o = align16(o + sizeof(int2) * 4 * ns);
+  L.w4 = o;        o = align16(o + sizeof(float4) * 4 * ns);
   const size_t xq_bytes = sizeof(float4) * 16 * (size_t)(M + 1);
   const size_t half = xq_bytes / 2;  // = the power tile, (M + 1) bins x 16 lanes x float2
   L.xbuf = o;      o = align16(o + xq_bytes);

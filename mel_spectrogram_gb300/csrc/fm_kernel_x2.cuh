@@ -8,8 +8,9 @@
 //             buffer, which is free from the end of pass 2 (the power tile
 //             uses the lower half) to the start of the next pass 1: the next
 //             tile lands during the split and the mel projection. TMA bulk
-//             copies (one per row, issued by warp 0, completing on an
-//             mbarrier) for interior tiles with 16-byte aligned rows,
+//             copies (one per row, dealt to one lane of every warp,
+//             completing on an mbarrier) for interior tiles with 16-byte
+//             aligned rows,
 //             cp.async element copies otherwise. Small shared memory per CTA
 //             (no separate input buffers) fits three CTAs per SM;
 //   tables  : window/offset, twiddles and filters are copied once per CTA
@@ -19,9 +20,9 @@
 //             one 16-byte store {re_a, re_b, im_a, im_b} per value;
 //   pass 2  : P-point DFTs for k2 = t and Q - t (role 0: 0 and Q/2), then the
 //             real-FFT split and |X|^p, still packed;
-//   power   : tile P[k][g] = (frame g, frame g + 16);
-//   mel     : lane = frame pair, half-warps on two filters, one packed FMA
-//             per filter weight for both frames.
+//   power   : tile rows P[k] of 32 frames, 16 bytes per 4 frames;
+//   mel     : quarter-warps on four filters, lane = 4 frames, two packed
+//             FMAs per filter weight.
 #pragma once
 
 #include "fm_fft2.cuh"
@@ -127,7 +128,8 @@ __device__ __forceinline__ void pass2_x2(const float4* xq_row, int t, cx2 (&a)[P
 __device__ __forceinline__ cx2 sel(bool c, const cx2& a, const cx2& b) { return c ? a : b; }
 
 // Real-FFT split of pass 2's outputs: both members of every pair (k, M - k)
-// are in this thread's registers; power pairs go to pw_col[k * 16] (float2).
+// are in this thread's registers; power pairs go to pw_col[k * 16] (float2,
+// 128-byte bin rows).
 //   role t >= 1: pairs (a[j], b[P-1-j]) at k = t + Q j, j < P;
 //   role 0:      pairs (a[j], a[(P-j) % P]) at k = Q j, j <= P/2 (j = 0 gives
 //                X[0] and X[M]), and (b[i], b[P-1-i]) at k = Q/2 + Q i, i < P/2.
@@ -176,42 +178,51 @@ __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], f
   }
 }
 
-// Mel projection over this warp's chunk stream (see X2Tables). Each chunk
-// adds two bins of one filter per half-warp: lane g takes frames g and g + 16
-// as a packed pair, the two weights arrive as one 16-byte broadcast of
-// duplicated pairs. Chunk flags start a sum and store it, so the loop has no
-// data-dependent bounds and runs kX2Unroll chunks per iteration with all
-// their loads in flight. Stores: 16 consecutive frames per half-warp, twice.
+// Mel projection over this warp's four chunk streams (see X2Tables). Lane
+// (h, l), h = lane / 8, runs stream h for frames l, l + 16, l + 8 and l + 24,
+// which one 16-byte load of a power-tile row gives (see split_x2): a chunk is
+// two such loads, one weight broadcast {w0, w0, w1, w1} and four packed FMAs.
+// The loop has no data-dependent bounds; it runs kX2Unroll chunks per
+// iteration with all their loads in flight. A chunk that ends its filter
+// stores the four sums (8 consecutive frames per quarter-warp per store) and
+// restarts them.
 template <typename OutT>
-__device__ __forceinline__ void mel_project_x2(const float2* s_pw2, const int4* __restrict__ s_chunks,
-                                               const float2* __restrict__ s_mw2, OutT* out_tile, int n_valid,
+__device__ __forceinline__ void mel_project_x2(const unsigned char* s_pw, const int2* __restrict__ s_desc,
+                                               const float4* __restrict__ s_w4, OutT* out_tile, int n_valid,
                                                long long n_frames, int c_begin, int c_end, int lane) {
-  const int g = lane & 15, h = lane >> 4;
-  const char* pcol = reinterpret_cast<const char*>(s_pw2 + g);
-  const char* wbase = reinterpret_cast<const char*>(s_mw2);
-  const bool va = g < n_valid, vb = g + kX2Lanes < n_valid;
-  float2 acc = make_float2(0.0f, 0.0f);
-  for (int c = c_begin; c < c_end; c += kX2Unroll) {
-    int4 d[kX2Unroll];
-    float4 w[kX2Unroll];
-    float2 p0[kX2Unroll], p1[kX2Unroll];
+  const int l = lane & 7, h = lane >> 3;
+  const unsigned char* pcol = s_pw + l * (int)sizeof(float4);
+  const bool v0 = l < n_valid, v1 = l + 16 < n_valid, v2 = l + 8 < n_valid, v3 = l + 24 < n_valid;
+  constexpr int kRow = kX2Lanes * (int)sizeof(float2);  // bytes per power-tile bin row
+  float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
+  const int2* dp = s_desc + 4 * c_begin + h;
+  const float4* wp = s_w4 + 4 * c_begin + h;
+  for (int c = c_begin; c < c_end; c += kX2Unroll, dp += 4 * kX2Unroll, wp += 4 * kX2Unroll) {
+    int2 d[kX2Unroll];
+    float4 w[kX2Unroll], p0[kX2Unroll], p1[kX2Unroll];
 #pragma unroll
-    for (int u = 0; u < kX2Unroll; ++u) d[u] = s_chunks[2 * (c + u) + h];
+    for (int u = 0; u < kX2Unroll; ++u) d[u] = dp[4 * u];
 #pragma unroll
     for (int u = 0; u < kX2Unroll; ++u) {
-      w[u] = *reinterpret_cast<const float4*>(wbase + d[u].y);
-      p0[u] = *reinterpret_cast<const float2*>(pcol + d[u].x);
-      p1[u] = *reinterpret_cast<const float2*>(pcol + d[u].x + kX2Lanes * (int)sizeof(float2));
+      w[u] = wp[4 * u];
+      p0[u] = *reinterpret_cast<const float4*>(pcol + d[u].x);
+      p1[u] = *reinterpret_cast<const float4*>(pcol + d[u].x + kRow);
     }
 #pragma unroll
     for (int u = 0; u < kX2Unroll; ++u) {
-      if (d[u].w & kChunkFirst) acc = make_float2(0.0f, 0.0f);
-      acc = fma2(make_float2(w[u].x, w[u].y), p0[u], acc);
-      acc = fma2(make_float2(w[u].z, w[u].w), p1[u], acc);
-      if (d[u].w & kChunkLast) {
-        OutT* o = out_tile + (long long)d[u].z * n_frames + g;
-        if (va) store_out(o, acc.x);
-        if (vb) store_out(o + kX2Lanes, acc.y);
+      const float2 w0 = make_float2(w[u].x, w[u].y), w1 = make_float2(w[u].z, w[u].w);
+      a01 = fma2(w0, make_float2(p0[u].x, p0[u].y), a01);
+      a23 = fma2(w0, make_float2(p0[u].z, p0[u].w), a23);
+      a01 = fma2(w1, make_float2(p1[u].x, p1[u].y), a01);
+      a23 = fma2(w1, make_float2(p1[u].z, p1[u].w), a23);
+      if (d[u].y >= 0) {
+        OutT* o = out_tile + (long long)d[u].y * n_frames + l;
+        if (v0) store_out(o, a01.x);
+        if (v1) store_out(o + 16, a01.y);
+        if (v2) store_out(o + 8, a23.x);
+        if (v3) store_out(o + 24, a23.y);
+        a01 = make_float2(0.0f, 0.0f);
+        a23 = make_float2(0.0f, 0.0f);
       }
     }
   }
@@ -226,13 +237,17 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const float4* s_p1 = reinterpret_cast<const float4*>(smem + lay.p1);
   const float4* s_twh4 = reinterpret_cast<const float4*>(smem + lay.tw_half);
   const float4* s_twf4 = reinterpret_cast<const float4*>(smem + lay.tw_full);
-  const int4* s_chunks = reinterpret_cast<const int4*>(smem + lay.chunks);
-  const float2* s_mw2 = reinterpret_cast<const float2*>(smem + lay.mel_w);
+  const int2* s_desc = reinterpret_cast<const int2*>(smem + lay.desc);
+  const float4* s_w4 = reinterpret_cast<const float4*>(smem + lay.w4);
   float4* s_xq = reinterpret_cast<float4*>(smem + lay.xbuf);
-  float2* s_pw2 = reinterpret_cast<float2*>(smem + lay.xbuf);  // aliases s_xq after pass 2
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = tid % kX2Lanes, role = tid / kX2Lanes;
+  // Power tile, aliasing s_xq after pass 2: bin rows of 128 bytes; within a
+  // row, 16 bytes per l < 8 hold frames {l, l + 16, l + 8, l + 24}, so thread
+  // g writes its pair (g, g + 16) at float2 slot 2 (g % 8) + g / 8.
+  const unsigned char* s_pw = smem + lay.xbuf;
+  float2* pw_col = reinterpret_cast<float2*>(smem + lay.xbuf) + 2 * (g & 7) + (g >> 3);
   const int esize = (int)sizeof(Raw);
   const int hop = HOP > 0 ? HOP : prm.hop, S = in_row_stride_x2(hop, esize), rows = in_rows(N, hop, kX2Frames);
   const Raw* in = static_cast<const Raw*>(prm.in);
@@ -320,9 +335,9 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     }
     const bool merged = role < 2;  // the warp that holds role 0 (and role 1)
     switch (prm.power_mode) {
-      case 0: split_x2<N, P, Q, 0>(za, zb, s_pw2 + g, s_twf4, role, prm.power, merged); break;
-      case 1: split_x2<N, P, Q, 1>(za, zb, s_pw2 + g, s_twf4, role, prm.power, merged); break;
-      default: split_x2<N, P, Q, 2>(za, zb, s_pw2 + g, s_twf4, role, prm.power, merged); break;
+      case 0: split_x2<N, P, Q, 0>(za, zb, pw_col, s_twf4, role, prm.power, merged); break;
+      case 1: split_x2<N, P, Q, 1>(za, zb, pw_col, s_twf4, role, prm.power, merged); break;
+      default: split_x2<N, P, Q, 2>(za, zb, pw_col, s_twf4, role, prm.power, merged); break;
     }
     __syncthreads();
 
@@ -331,10 +346,10 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     const long long obase = cur.b * prm.n_mels * (long long)prm.n_frames + t0;
     cur = nxt;
     if (prm.out_dtype == FM_F32)
-      mel_project_x2(s_pw2, s_chunks, s_mw2, static_cast<float*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
+      mel_project_x2(s_pw, s_desc, s_w4, static_cast<float*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
                      s_end, lane);
     else
-      mel_project_x2(s_pw2, s_chunks, s_mw2, static_cast<__half*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
+      mel_project_x2(s_pw, s_desc, s_w4, static_cast<__half*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
                      s_end, lane);
   }
   cp_async_commit();  // nothing may stay in flight past the end of the CTA
@@ -349,7 +364,7 @@ __global__ void __launch_bounds__(P* kX2Lanes, 3) mel_kernel_x2(const KernelPara
   static_assert(THREADS % 32 == 0, "CTA must be whole warps");
   extern __shared__ __align__(16) unsigned char smem[];
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
-  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, prm.x2_chunks, prm.x2_w, esize);
+  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, prm.x2_slots, esize);
   pdl_launch_dependents();
   // tables, fetched once per CTA in the first tile's cp.async group
   const int tid = threadIdx.x;
@@ -357,8 +372,8 @@ __global__ void __launch_bounds__(P* kX2Lanes, 3) mel_kernel_x2(const KernelPara
   copy_table_async(smem + lay.p1, t->p1, (int)sizeof(float4) * M, tid, THREADS);
   copy_table_async(smem + lay.tw_half, t->tw_half, (int)sizeof(float4) * M, tid, THREADS);
   copy_table_async(smem + lay.tw_full, t->tw_full, (int)sizeof(float4) * (M + 1), tid, THREADS);
-  copy_table_async(smem + lay.chunks, t->chunk, (int)sizeof(int4) * 2 * prm.x2_chunks, tid, THREADS);
-  copy_table_async(smem + lay.mel_w, t->mel_w, (int)sizeof(float2) * prm.x2_w, tid, THREADS);
+  copy_table_async(smem + lay.desc, t->desc, (int)sizeof(int2) * 4 * prm.x2_slots, tid, THREADS);
+  copy_table_async(smem + lay.w4, t->w4, (int)sizeof(float4) * 4 * prm.x2_slots, tid, THREADS);
   if (prm.in_dtype == FM_F32) run_tiles_x2<N, P, Q, HOP, float>(prm, smem, lay);
   else if (prm.in_dtype == FM_I16) run_tiles_x2<N, P, Q, HOP, short>(prm, smem, lay);
   else run_tiles_x2<N, P, Q, HOP, __half>(prm, smem, lay);
