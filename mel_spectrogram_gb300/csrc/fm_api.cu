@@ -171,7 +171,7 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
   const int in_esize = in_dtype == FM_F32 ? 4 : 2;
   const size_t smem_total =
-      var->kind == 1 ? fm::smem_layout_x2(n_fft, hop, x2_slots, in_esize).total
+      var->kind == 1 ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize).total
                      : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
   if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_slots > fm::kX2MaxSlots ||
                          var->threads / 32 > fm::kX2MaxWarps))

@@ -103,14 +103,19 @@ struct X2Tables {
   float4 w4[kX2MaxSlots][4];
 };
 
-// Row stride (elements) of the packed kernel's staged tile: each row starts
-// on a 16-byte boundary (TMA bulk copies need it) and the stride is an odd
-// multiple of 16 bytes, so the per-frame pair reads of 16 lanes spread over
-// 8 bank groups (two lanes per group).
-__host__ __device__ constexpr int in_row_stride_x2_c(int hop, int esize) {
-  return ((((hop + 16 / esize - 1) / (16 / esize)) | 1) * (16 / esize));
+// Line stride (elements) of the packed kernel's staged tile, for lines of
+// `len` samples: each line starts on a 16-byte boundary (TMA bulk copies need
+// it) and the stride is an odd multiple of 16 bytes. With 4-byte samples the
+// frame starts of a half-warp's 16 lanes then fall on 8 distinct 16-byte bank
+// groups, two lanes each, and the warp's two half-warps (8 bytes apart) read
+// their 256 bytes in the minimum two wavefronts. That holds for lines of one
+// hop (frame g on line g) and of two hops when the hop is a multiple of 32
+// words (frames 2j and 2j + 1 on line j, 0 mod 32 banks apart). 2-byte
+// samples take two wavefronts for 128 bytes either way.
+__host__ __device__ constexpr int in_row_stride_x2_c(int len, int esize) {
+  return ((((len + 16 / esize - 1) / (16 / esize)) | 1) * (16 / esize));
 }
-__host__ __device__ inline int in_row_stride_x2(int hop, int esize) { return in_row_stride_x2_c(hop, esize); }
+__host__ __device__ inline int in_row_stride_x2(int len, int esize) { return in_row_stride_x2_c(len, esize); }
 
 // Layout of the two-frames-per-thread kernel (32-frame tiles): its tables
 // (copied once per CTA from the X2Tables block) and the exchange buffer. The
@@ -122,8 +127,14 @@ struct SmemLayoutX2 {
   size_t bars, p1, tw_half, tw_full, desc, w4, xbuf, in_tile, in_tile_bytes, total;
 };
 
+// Staged lines of the packed kernel: k_hops hops of samples per line (2 for
+// a compile-time hop, else 1), `lines` of them per 32-frame tile.
+__host__ __device__ inline int x2_lines(int n_fft, int hop, int k_hops) {
+  return (in_rows(n_fft, hop, 32) + k_hops - 1) / k_hops;
+}
+
 // n_slots: mel chunk slots (four chunks each)
-__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n_slots, int in_esize) {
+__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int k_hops, int n_slots, int in_esize) {
   const int M = n_fft / 2;
   const int ns = n_slots > 0 ? n_slots : 1;
   SmemLayoutX2 L;
@@ -137,7 +148,8 @@ __host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int n
   const size_t xq_bytes = sizeof(float4) * 16 * (size_t)(M + 1);
   const size_t half = xq_bytes / 2;  // = the power tile, (M + 1) bins x 16 lanes x float2
   L.xbuf = o;      o = align16(o + xq_bytes);
-  L.in_tile_bytes = align16((size_t)in_esize * in_rows(n_fft, hop, 32) * in_row_stride_x2(hop, in_esize));
+  L.in_tile_bytes =
+      align16((size_t)in_esize * x2_lines(n_fft, hop, k_hops) * in_row_stride_x2(k_hops * hop, in_esize));
   if (L.in_tile_bytes <= xq_bytes - align16(half)) {
     L.in_tile = L.xbuf + align16(half);
   } else {

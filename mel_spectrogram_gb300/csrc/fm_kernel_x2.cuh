@@ -4,13 +4,13 @@
 // Same path and same four-step real FFT as fm_kernel.cuh, but a tile holds 32
 // frames and thread (role, g), g < 16, carries frames g and g + 16 through
 // every phase as packed pairs (see fm_fft2.cuh):
-//   staging : raw samples as rows of `hop` in the upper half of the exchange
-//             buffer, which is free from the end of pass 2 (the power tile
-//             uses the lower half) to the start of the next pass 1: the next
-//             tile lands during the split and the mel projection. TMA bulk
-//             copies (one per row, dealt to one lane of every warp,
-//             completing on an mbarrier) for interior tiles with 16-byte
-//             aligned rows,
+//   staging : raw samples in lines of two hops (one when the hop is a
+//             runtime value) in the upper half of the exchange buffer,
+//             which is free from the end of pass 2 (the power tile uses the
+//             lower half) to the start of the next pass 1: the next tile
+//             lands during the split and the mel projection. TMA bulk copies
+//             (one per line, dealt to one lane of every warp, completing on
+//             an mbarrier) for interior tiles with 16-byte aligned lines,
 //             cp.async element copies otherwise. Small shared memory per CTA
 //             (no separate input buffers) fits three CTAs per SM;
 //   tables  : window/offset, twiddles and filters are copied once per CTA
@@ -34,34 +34,40 @@ constexpr int kX2Lanes = 16;   // lanes per role
 constexpr int kX2Frames = 32;  // frames per tile
 
 // Pass 1, load half: the windowed pairs z[q] = (y[2n], y[2n+1]) / 2 with
-// n = p + P q, for frames g and g + 16 (frame base pointers base_a and
-// base_a + 16 rows). HOP > 0: the hop is a compile-time multiple of 2P, so the
-// tile offset of the pair is (2Pq / HOP) rows + (2Pq mod HOP) + 2p, a
-// compile-time constant plus 2p, and the loads need no address math.
+// n = p + P q, for frames g and g + 16. HOP > 0: the hop is a compile-time
+// multiple of 2P and the tile is staged in lines of two hops, frame g starting
+// at line g / 2, column (g % 2) HOP; base points at sample 2p of frame g and
+// base_o is base plus one line pad for odd g. The line crossings of sample
+// 2Pq + 2p do not depend on p, so every load is a compile-time offset from
+// base or base_o (frame g + 16 is 8 lines further). HOP = 0: lines of one hop,
+// frame g on line g, and the offsets come from the table.
 template <int P, int Q, int HOP, typename Raw>
-__device__ __forceinline__ void pass1_load_x2(const Raw* __restrict__ base_a, int S, const float4* __restrict__ s_p1,
-                                              int p, cx2 (&z)[Q]) {
+__device__ __forceinline__ void pass1_load_x2(const Raw* __restrict__ base, const Raw* __restrict__ base_o, int S,
+                                              const float4* __restrict__ s_p1, int p, cx2 (&z)[Q]) {
   const float4* tab = s_p1 + p * Q;
   if constexpr (HOP > 0) {
     static_assert(HOP % (2 * P) == 0, "compile-time hop must be a multiple of 2P");
-    constexpr int SC = in_row_stride_x2_c(HOP, (int)sizeof(Raw));
-    const Raw* base = base_a + 2 * p;
+    constexpr int SC = in_row_stride_x2_c(2 * HOP, (int)sizeof(Raw));
+    constexpr int PAD = SC - 2 * HOP;
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
       const float2 w = *reinterpret_cast<const float2*>(tab + q);
-      const int off = (2 * P * q / HOP) * SC + (2 * P * q) % HOP;
-      const float2 va = load_pair(base + off);
-      const float2 vb = load_pair(base + off + kX2Lanes * SC);
+      const int j = 2 * P * q;
+      const int ce = j / (2 * HOP), co = (HOP + j) / (2 * HOP);  // lines crossed, even / odd g
+      const Raw* b = co != ce ? base_o : base;
+      const int off = j + ce * PAD;
+      const float2 va = load_pair(b + off);
+      const float2 vb = load_pair(b + off + (kX2Lanes / 2) * SC);
       z[q].re = make_float2(va.x * w.x, vb.x * w.x);
       z[q].im = make_float2(va.y * w.y, vb.y * w.y);
     }
   } else {
-    const Raw* base_b = base_a + kX2Lanes * S;
+    const Raw* base_b = base + kX2Lanes * S;
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
       const float4 e = tab[q];
       const int off = __float_as_int(e.z);
-      const float2 va = load_pair(base_a + off);
+      const float2 va = load_pair(base + off);
       const float2 vb = load_pair(base_b + off);
       z[q].re = make_float2(va.x * e.x, vb.x * e.x);
       z[q].im = make_float2(va.y * e.y, vb.y * e.y);
@@ -249,7 +255,9 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const unsigned char* s_pw = smem + lay.xbuf;
   float2* pw_col = reinterpret_cast<float2*>(smem + lay.xbuf) + 2 * (g & 7) + (g >> 3);
   const int esize = (int)sizeof(Raw);
-  const int hop = HOP > 0 ? HOP : prm.hop, S = in_row_stride_x2(hop, esize), rows = in_rows(N, hop, kX2Frames);
+  constexpr int KH = HOP > 0 ? 2 : 1;  // hops per staged line
+  const int hop = HOP > 0 ? HOP : prm.hop, line = KH * hop;
+  const int S = in_row_stride_x2(line, esize), rows = x2_lines(N, hop, KH);
   const Raw* in = static_cast<const Raw*>(prm.in);
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
@@ -268,7 +276,7 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     split(tile, pl.b, pl.tt);
     pl.gstart = (long long)pl.tt * kX2Frames * hop - prm.pad;
     const Raw* src = in + pl.b * T;
-    pl.tma = pl.gstart >= 0 && pl.gstart + (long long)rows * hop <= T && ((hop * esize) & 15) == 0 &&
+    pl.tma = pl.gstart >= 0 && pl.gstart + (long long)rows * line <= T && ((hop * esize) & 15) == 0 &&
              (reinterpret_cast<uintptr_t>(src + pl.gstart) & 15) == 0;
     return pl;
   };
@@ -278,19 +286,22 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   // last written through the generic proxy (exchange stores), hence the proxy
   // fence before each issuing lane's first copy.
   Raw* s_in = reinterpret_cast<Raw*>(smem + lay.in_tile);
+  // frame g's first sample (HOP > 0: plus 2p, the role's first pair)
+  const Raw* fbase = HOP > 0 ? s_in + (g >> 1) * S + (g & 1) * hop + 2 * role : s_in + g * S;
+  const Raw* fbase_o = fbase + ((HOP > 0 && (g & 1)) ? S - line : 0);
   auto stage = [&](const Place& pl) {
     const Raw* src = in + pl.b * T;
     if (pl.tma) {
       // The barrier's single arrival carries the byte count, so its phase
       // cannot complete before it even if some copies land first.
-      if (tid == 0) mbar_arrive_expect_tx(&bars[0], (unsigned)(rows * hop * esize));
+      if (tid == 0) mbar_arrive_expect_tx(&bars[0], (unsigned)(rows * line * esize));
       if (lane == 0) {
         fence_proxy_async();
         for (int r = warp; r < rows; r += NWARPS)
-          tma_load_1d(s_in + r * S, src + pl.gstart + (long long)r * hop, (unsigned)(hop * esize), &bars[0]);
+          tma_load_1d(s_in + r * S, src + pl.gstart + (long long)r * line, (unsigned)(line * esize), &bars[0]);
       }
     } else {
-      stage_tile<Raw, NWARPS>(src, T, pl.gstart, rows, hop, S, s_in, warp, lane);
+      stage_tile<Raw, NWARPS>(src, T, pl.gstart, rows, line, S, s_in, warp, lane);
     }
     cp_async_commit();
   };
@@ -319,7 +330,7 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
 
     float4* xq_row = s_xq + g * GS4;
     cx2 z[Q];
-    pass1_load_x2<P, Q, HOP, Raw>(s_in + g * S, S, s_p1, role, z);
+    pass1_load_x2<P, Q, HOP, Raw>(fbase, fbase_o, S, s_p1, role, z);
     __syncthreads();  // samples are in registers: the exchange buffer (holding them) may be overwritten
     pass1_finish_x2<P, Q>(z, s_twh4, xq_row, role);
     __syncthreads();
@@ -364,7 +375,7 @@ __global__ void __launch_bounds__(P* kX2Lanes, 3) mel_kernel_x2(const KernelPara
   static_assert(THREADS % 32 == 0, "CTA must be whole warps");
   extern __shared__ __align__(16) unsigned char smem[];
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
-  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, prm.x2_slots, esize);
+  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, HOP > 0 ? 2 : 1, prm.x2_slots, esize);
   pdl_launch_dependents();
   // tables, fetched once per CTA in the first tile's cp.async group
   const int tid = threadIdx.x;
