@@ -162,7 +162,8 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   }
   const int nnz = (int)mw.size();
   X2Schedule x2s;
-  if (var->kind == 1) x2s = build_x2_schedule(n_fft / 2, n_mels, var->threads / 32, ms, ml, mo, mw);
+  const int x2_warps = var->threads / 32 / fm::kX2Groups;  // warps per tile group of the packed kernel
+  if (var->kind == 1) x2s = build_x2_schedule(n_fft / 2, n_mels, x2_warps, ms, ml, mo, mw);
   const int x2_slots = var->kind == 1 ? x2s.warp_begin.back() : 0;
 
   int dev = 0;
@@ -171,10 +172,10 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
   const int in_esize = in_dtype == FM_F32 ? 4 : 2;
   const size_t smem_total =
-      var->kind == 1 ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize).total
+      var->kind == 1 ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize, fm::kX2Groups).total
                      : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
   if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_slots > fm::kX2MaxSlots ||
-                         var->threads / 32 > fm::kX2MaxWarps))
+                         x2_warps > fm::kX2MaxWarps))
     return FM_ERR_UNSUPPORTED;
   if (smem_total > (size_t)prop.sharedMemPerBlockOptin) return FM_ERR_UNSUPPORTED;
   // allow the device maximum once, so plans of different sizes never undercut each other
@@ -253,7 +254,9 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   if (var->kind == 1) {
     fm::X2Tables* t = reinterpret_cast<fm::X2Tables*>(blob.data() + o_x2);
     std::memcpy(t->p1, p1.data(), sizeof(float4) * M);
-    std::memcpy(t->tw_half, twh4.data(), sizeof(float4) * M);
+    // pass-1 twiddles by role: [p * Q + k2] = W_M^{p k2}
+    for (int pp = 0; pp < var->P; ++pp)
+      for (int k2 = 0; k2 < var->Q; ++k2) t->tw_half[pp * var->Q + k2] = twh4[pp * k2];
     std::memcpy(t->tw_full, twf4.data(), sizeof(float4) * (M + 1));
     for (size_t i = 0; i < x2s.warp_begin.size(); ++i) t->warp_begin[i] = x2s.warp_begin[i];
     std::memcpy(t->desc, x2s.desc.data(), sizeof(int2) * x2s.desc.size());

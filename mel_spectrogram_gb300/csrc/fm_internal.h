@@ -83,10 +83,11 @@ constexpr int kX2MaxM = 200;
 constexpr int kX2MaxMels = 256;
 constexpr int kX2MaxWarps = 16;
 constexpr int kX2Unroll = 4;    // chunks per unrolled mel iteration
+constexpr int kX2Groups = 3;    // independent tile groups per CTA (one CTA per SM)
 constexpr int kX2MaxSlots = 1024;  // mel chunk slots (4 chunks each) over all warps
 struct X2Tables {
   float4 p1[kX2MaxM];        // as KernelParams::p1
-  float4 tw_half[kX2MaxM];   // {c, c, d, d}, W_M^j = c + i d
+  float4 tw_half[kX2MaxM];   // [p * Q + k2] = W_M^{p k2} as {c, c, d, d}, W = c + i d
   float4 tw_full[kX2MaxM + 1];
   // Mel work as four chunk streams per warp, one per quarter-warp. Every
   // filter is padded to an even length L >= 2 (zero weights; a run that would
@@ -124,7 +125,9 @@ __host__ __device__ inline int in_row_stride_x2(int len, int esize) { return in_
 // needs no separate input buffer (when a tile fits there; otherwise one is
 // appended).
 struct SmemLayoutX2 {
-  size_t bars, p1, tw_half, tw_full, desc, w4, xbuf, in_tile, in_tile_bytes, total;
+  // group g's mbarrier at bars + 8 g, its exchange buffer at xbuf + g group_stride
+  // and its staged tile at in_tile + g group_stride
+  size_t bars, p1, tw_half, tw_full, desc, w4, xbuf, in_tile, in_tile_bytes, group_stride, total;
 };
 
 // Staged lines of the packed kernel: k_hops hops of samples per line (2 for
@@ -133,30 +136,33 @@ __host__ __device__ inline int x2_lines(int n_fft, int hop, int k_hops) {
   return (in_rows(n_fft, hop, 32) + k_hops - 1) / k_hops;
 }
 
-// n_slots: mel chunk slots (four chunks each)
-__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int k_hops, int n_slots, int in_esize) {
+// n_slots: mel chunk slots (four chunks each); groups: tile groups per CTA,
+// which share the tables and own one exchange buffer (and tile) each
+__host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int k_hops, int n_slots, int in_esize,
+                                                       int groups) {
   const int M = n_fft / 2;
   const int ns = n_slots > 0 ? n_slots : 1;
   SmemLayoutX2 L;
   size_t o = 0;
-  L.bars = o;      o = align16(o + 2 * sizeof(unsigned long long));
+  L.bars = o;      o = align16(o + sizeof(unsigned long long) * groups);
   L.p1 = o;        o = align16(o + sizeof(float4) * M);
   L.tw_half = o;   o = align16(o + sizeof(float4) * M);
   L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));
   L.desc = o;      o = align16(o + sizeof(int2) * 4 * ns);
   L.w4 = o;        o = align16(o + sizeof(float4) * 4 * ns);
-  const size_t xq_bytes = sizeof(float4) * 16 * (size_t)(M + 1);
-  const size_t half = xq_bytes / 2;  // = the power tile, (M + 1) bins x 16 lanes x float2
-  L.xbuf = o;      o = align16(o + xq_bytes);
+  const size_t xq_bytes = align16(sizeof(float4) * 16 * (size_t)(M + 1));
+  const size_t half = align16(xq_bytes / 2);  // >= the power tile, (M + 1) bins x 16 lanes x float2
+  L.xbuf = o;
   L.in_tile_bytes =
       align16((size_t)in_esize * x2_lines(n_fft, hop, k_hops) * in_row_stride_x2(k_hops * hop, in_esize));
-  if (L.in_tile_bytes <= xq_bytes - align16(half)) {
-    L.in_tile = L.xbuf + align16(half);
+  if (L.in_tile_bytes <= xq_bytes - half) {
+    L.in_tile = L.xbuf + half;
+    L.group_stride = xq_bytes;
   } else {
-    L.in_tile = o;
-    o += L.in_tile_bytes;
+    L.in_tile = L.xbuf + xq_bytes;
+    L.group_stride = xq_bytes + L.in_tile_bytes;
   }
-  L.total = o;
+  L.total = L.xbuf + groups * L.group_stride;
   return L;
 }
 

@@ -33,6 +33,19 @@ namespace fm {
 constexpr int kX2Lanes = 16;   // lanes per role
 constexpr int kX2Frames = 32;  // frames per tile
 
+// Barrier over one tile group (named barrier `id`, `n` threads), and the same
+// with an OR vote over the group's threads.
+__device__ __forceinline__ void group_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ bool group_sync_or(int id, int n, bool v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((int)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // Pass 1, load half: the windowed pairs z[q] = (y[2n], y[2n+1]) / 2 with
 // n = p + P q, for frames g and g + 16. HOP > 0: the hop is a compile-time
 // multiple of 2P and the tile is staged in lines of two hops, frame g starting
@@ -81,11 +94,12 @@ __device__ __forceinline__ void pass1_load_x2(const Raw* __restrict__ base, cons
 template <int P, int Q>
 __device__ __forceinline__ void pass1_finish_x2(cx2 (&z)[Q], const float4* __restrict__ s_twh4, float4* xq_row,
                                                 int p) {
+  const float4* tw = s_twh4 + p * Q;  // this role's W_M^{p k2}, k2 < Q
   dft<Q>(z);
   xq_row[p] = make_float4(z[0].re.x, z[0].re.y, z[0].im.x, z[0].im.y);
 #pragma unroll
   for (int k2 = 1; k2 < Q; ++k2) {
-    const float4 w = s_twh4[p * k2];
+    const float4 w = tw[k2];
     const cx2 v = cmul(z[k2], make_float2(w.x, w.y), make_float2(w.z, w.w));
     xq_row[k2 * P + p] = make_float4(v.re.x, v.re.y, v.im.x, v.im.y);
   }
@@ -234,10 +248,14 @@ __device__ __forceinline__ void mel_project_x2(const unsigned char* s_pw, const 
   }
 }
 
+// The tile loop of one group: group `grp` of the CTA runs virtual tile slot
+// blockIdx.x + gridDim.x * grp, stepping by gridDim.x * kX2Groups, with its
+// own exchange buffer, staged tile, mbarrier and named barrier 1 + grp.
 template <int N, int P, int Q, int HOP, typename Raw>
-__device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay) {
+__device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay,
+                                             int grp) {
   constexpr int M = N / 2;
-  constexpr int THREADS = P * kX2Lanes;
+  constexpr int THREADS = P * kX2Lanes;  // per group
   constexpr int NWARPS = THREADS / 32;
   constexpr int GS4 = M + 1;  // float4 stride between frame pairs in the exchange buffer (odd)
   const float4* s_p1 = reinterpret_cast<const float4*>(smem + lay.p1);
@@ -245,15 +263,17 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const float4* s_twf4 = reinterpret_cast<const float4*>(smem + lay.tw_full);
   const int2* s_desc = reinterpret_cast<const int2*>(smem + lay.desc);
   const float4* s_w4 = reinterpret_cast<const float4*>(smem + lay.w4);
-  float4* s_xq = reinterpret_cast<float4*>(smem + lay.xbuf);
+  unsigned char* s_x = smem + lay.xbuf + grp * lay.group_stride;
+  float4* s_xq = reinterpret_cast<float4*>(s_x);
+  const int bar_id = 1 + grp;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x - grp * THREADS, warp = tid >> 5, lane = tid & 31;
   const int g = tid % kX2Lanes, role = tid / kX2Lanes;
   // Power tile, aliasing s_xq after pass 2: bin rows of 128 bytes; within a
   // row, 16 bytes per l < 8 hold frames {l, l + 16, l + 8, l + 24}, so thread
   // g writes its pair (g, g + 16) at float2 slot 2 (g % 8) + g / 8.
-  const unsigned char* s_pw = smem + lay.xbuf;
-  float2* pw_col = reinterpret_cast<float2*>(smem + lay.xbuf) + 2 * (g & 7) + (g >> 3);
+  const unsigned char* s_pw = s_x;
+  float2* pw_col = reinterpret_cast<float2*>(s_x) + 2 * (g & 7) + (g >> 3);
   const int esize = (int)sizeof(Raw);
   constexpr int KH = HOP > 0 ? 2 : 1;  // hops per staged line
   const int hop = HOP > 0 ? HOP : prm.hop, line = KH * hop;
@@ -262,22 +282,23 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
   const int s_begin = __ldg(&prm.x2->warp_begin[warp]), s_end = __ldg(&prm.x2->warp_begin[warp + 1]);
-  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + lay.bars);
+  unsigned long long* bar = reinterpret_cast<unsigned long long*>(smem + lay.bars) + grp;
   // Where a tile lives: signal b, tile index tt within it, signal index of
   // tile position 0, and whether it is interior with 16-byte aligned rows
   // (then TMA bulk copies stage it). Computed once per tile and carried.
   struct Place {
-    long long b, gstart;
+    long long b;
     int tt;
     bool tma;
   };
+  auto first_sample = [&](const Place& pl) { return (long long)pl.tt * kX2Frames * hop - prm.pad; };
   auto locate = [&](long long tile) {
     Place pl;
     split(tile, pl.b, pl.tt);
-    pl.gstart = (long long)pl.tt * kX2Frames * hop - prm.pad;
+    const long long gstart = first_sample(pl);
     const Raw* src = in + pl.b * T;
-    pl.tma = pl.gstart >= 0 && pl.gstart + (long long)rows * line <= T && ((hop * esize) & 15) == 0 &&
-             (reinterpret_cast<uintptr_t>(src + pl.gstart) & 15) == 0;
+    pl.tma = gstart >= 0 && gstart + (long long)rows * line <= T && ((hop * esize) & 15) == 0 &&
+             (reinterpret_cast<uintptr_t>(src + gstart) & 15) == 0;
     return pl;
   };
   // Stage a tile into the input area: TMA row copies issued by one lane of
@@ -285,64 +306,73 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   // cp.async element copies by all threads at the signal edges. The area was
   // last written through the generic proxy (exchange stores), hence the proxy
   // fence before each issuing lane's first copy.
-  Raw* s_in = reinterpret_cast<Raw*>(smem + lay.in_tile);
+  Raw* s_in = reinterpret_cast<Raw*>(smem + lay.in_tile + grp * lay.group_stride);
   // frame g's first sample (HOP > 0: plus 2p, the role's first pair)
   const Raw* fbase = HOP > 0 ? s_in + (g >> 1) * S + (g & 1) * hop + 2 * role : s_in + g * S;
   const Raw* fbase_o = fbase + ((HOP > 0 && (g & 1)) ? S - line : 0);
   auto stage = [&](const Place& pl) {
-    const Raw* src = in + pl.b * T;
+    const Raw* src = in + pl.b * T + first_sample(pl);
     if (pl.tma) {
       // The barrier's single arrival carries the byte count, so its phase
       // cannot complete before it even if some copies land first.
-      if (tid == 0) mbar_arrive_expect_tx(&bars[0], (unsigned)(rows * line * esize));
+      if (tid == 0) mbar_arrive_expect_tx(bar, (unsigned)(rows * line * esize));
       if (lane == 0) {
         fence_proxy_async();
         for (int r = warp; r < rows; r += NWARPS)
-          tma_load_1d(s_in + r * S, src + pl.gstart + (long long)r * line, (unsigned)(line * esize), &bars[0]);
+          tma_load_1d(s_in + r * S, src + (long long)r * line, (unsigned)(line * esize), bar);
       }
     } else {
-      stage_tile<Raw, NWARPS>(src, T, pl.gstart, rows, line, S, s_in, warp, lane);
+      stage_tile<Raw, NWARPS>(in + pl.b * T, T, first_sample(pl), rows, line, S, s_in, warp, lane);
     }
     cp_async_commit();
   };
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
+    mbar_init(bar, 1);
     fence_mbar_init();
   }
-  __syncthreads();  // the barrier exists before anyone polls it
+  __syncthreads();  // the barriers exist before anyone polls them
   pdl_wait();       // caller buffers only after the previous kernel in the stream is done
   unsigned phase = 0u;
 
-  long long tile = blockIdx.x;
+  long long tile = blockIdx.x + (long long)gridDim.x * grp;
   Place cur = locate(tile);
   if (tile < prm.total_tiles) stage(cur);
-  for (; tile < prm.total_tiles; tile += gridDim.x) {
+  // the tables (copied by every thread of the CTA) and this thread's first
+  // cp.async copies are complete and visible to all groups
+  cp_async_wait_all();
+  __syncthreads();
+  for (; tile < prm.total_tiles; tile += (long long)gridDim.x * kX2Groups) {
     cp_async_wait_all();
     bool failed = false;
     if (cur.tma) {
       // one thread waits for the copies; the barrier below then orders them
-      // for the whole CTA while the other warps sleep instead of polling
-      if (tid == 0) failed = !mbar_wait_bounded(&bars[0], phase, prm.err);
+      // for the whole group while the other warps sleep instead of polling
+      if (tid == 0) failed = !mbar_wait_bounded(bar, phase, prm.err);
       phase ^= 1u;
     }
     // this tile's samples are visible; the previous tile's mel phase is done
-    if (__syncthreads_or(failed)) return;  // a staging copy never arrived (error recorded)
+    if (group_sync_or(bar_id, THREADS, failed)) return;  // a staging copy never arrived (error recorded)
 
     float4* xq_row = s_xq + g * GS4;
     cx2 z[Q];
     pass1_load_x2<P, Q, HOP, Raw>(fbase, fbase_o, S, s_p1, role, z);
-    __syncthreads();  // samples are in registers: the exchange buffer (holding them) may be overwritten
+    group_sync(bar_id, THREADS);  // samples are in registers: the exchange buffer (holding them) may be overwritten
     pass1_finish_x2<P, Q>(z, s_twh4, xq_row, role);
-    __syncthreads();
+    group_sync(bar_id, THREADS);
 
     cx2 za[P], zb[P];
     pass2_x2<P, Q>(xq_row, role, za, zb);
-    __syncthreads();  // exchange reads done: power tile (lower half) and next tile (upper half) may land
-    const long long next = tile + gridDim.x;
-    Place nxt{};
+    group_sync(bar_id, THREADS);  // exchange reads done: power tile (lower half) and next tile (upper half) may land
+    // this tile's output place; then the next tile starts landing during the
+    // split and the mel projection
+    const int t0 = cur.tt * kX2Frames;
+    const int n_valid = min(kX2Frames, prm.n_frames - t0);
+    const long long obase = cur.b * prm.n_mels * (long long)prm.n_frames + t0;
+    const long long next = tile + (long long)gridDim.x * kX2Groups;
+    cur = Place{};
     if (next < prm.total_tiles) {
-      nxt = locate(next);
-      stage(nxt);  // lands during the split and the mel projection
+      cur = locate(next);
+      stage(cur);
     }
     const bool merged = role < 2;  // the warp that holds role 0 (and role 1)
     switch (prm.power_mode) {
@@ -350,12 +380,8 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
       case 1: split_x2<N, P, Q, 1>(za, zb, pw_col, s_twf4, role, prm.power, merged); break;
       default: split_x2<N, P, Q, 2>(za, zb, pw_col, s_twf4, role, prm.power, merged); break;
     }
-    __syncthreads();
+    group_sync(bar_id, THREADS);
 
-    const int t0 = cur.tt * kX2Frames;
-    const int n_valid = min(kX2Frames, prm.n_frames - t0);
-    const long long obase = cur.b * prm.n_mels * (long long)prm.n_frames + t0;
-    cur = nxt;
     if (prm.out_dtype == FM_F32)
       mel_project_x2(s_pw, s_desc, s_w4, static_cast<float*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
                      s_end, lane);
@@ -367,17 +393,21 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   cp_async_wait_all();
 }
 
+// One CTA per SM: kX2Groups groups of P x 16 threads, each running its own
+// tile loop on its own exchange buffer; the tables are shared.
 template <int N, int P, int Q, int HOP>
-__global__ void __launch_bounds__(P* kX2Lanes, 3) mel_kernel_x2(const KernelParams prm) {
+__global__ void __launch_bounds__(kX2Groups* P* kX2Lanes, 1) mel_kernel_x2(const KernelParams prm) {
   constexpr int M = N / 2;
-  constexpr int THREADS = P * kX2Lanes;
+  constexpr int GROUP = P * kX2Lanes;
+  constexpr int THREADS = kX2Groups * GROUP;
   static_assert(P * Q == M && Q == 2 * P && M <= kX2MaxM, "x2 kernel needs Q = 2P and M <= 200");
-  static_assert(THREADS % 32 == 0, "CTA must be whole warps");
+  static_assert(GROUP % 32 == 0, "a group must be whole warps");
   extern __shared__ __align__(16) unsigned char smem[];
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
-  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, HOP > 0 ? 2 : 1, prm.x2_slots, esize);
+  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, HOP > 0 ? 2 : 1, prm.x2_slots, esize, kX2Groups);
   pdl_launch_dependents();
-  // tables, fetched once per CTA in the first tile's cp.async group
+  // tables, fetched once per CTA; every thread waits for its copies before
+  // the CTA-wide barrier that precedes the tile loops
   const int tid = threadIdx.x;
   const X2Tables* t = prm.x2;
   copy_table_async(smem + lay.p1, t->p1, (int)sizeof(float4) * M, tid, THREADS);
@@ -385,9 +415,12 @@ __global__ void __launch_bounds__(P* kX2Lanes, 3) mel_kernel_x2(const KernelPara
   copy_table_async(smem + lay.tw_full, t->tw_full, (int)sizeof(float4) * (M + 1), tid, THREADS);
   copy_table_async(smem + lay.desc, t->desc, (int)sizeof(int2) * 4 * prm.x2_slots, tid, THREADS);
   copy_table_async(smem + lay.w4, t->w4, (int)sizeof(float4) * 4 * prm.x2_slots, tid, THREADS);
-  if (prm.in_dtype == FM_F32) run_tiles_x2<N, P, Q, HOP, float>(prm, smem, lay);
-  else if (prm.in_dtype == FM_I16) run_tiles_x2<N, P, Q, HOP, short>(prm, smem, lay);
-  else run_tiles_x2<N, P, Q, HOP, __half>(prm, smem, lay);
+  // warp-uniform (a group is whole warps); reading it through a shuffle lets
+  // the compiler keep the group's base addresses in uniform registers
+  const int grp = __shfl_sync(0xffffffffu, tid / GROUP, 0);
+  if (prm.in_dtype == FM_F32) run_tiles_x2<N, P, Q, HOP, float>(prm, smem, lay, grp);
+  else if (prm.in_dtype == FM_I16) run_tiles_x2<N, P, Q, HOP, short>(prm, smem, lay, grp);
+  else run_tiles_x2<N, P, Q, HOP, __half>(prm, smem, lay, grp);
 }
 
 }  // namespace fm
@@ -397,6 +430,6 @@ __global__ void __launch_bounds__(P* kX2Lanes, 3) mel_kernel_x2(const KernelPara
 #define FM_DEFINE_VARIANT_X2(NAME, N, P, Q, HOP)                                              \
   namespace fm {                                                                              \
   template __global__ void mel_kernel_x2<N, P, Q, HOP>(const KernelParams);                  \
-  extern const Variant NAME = {N, P, Q, kX2Frames, P * kX2Lanes, 2, 1,                         \
+  extern const Variant NAME = {N, P, Q, kX2Frames, kX2Groups * P * kX2Lanes, 2, 1,             \
                                (const void*)&mel_kernel_x2<N, P, Q, HOP>, HOP};               \
   }
