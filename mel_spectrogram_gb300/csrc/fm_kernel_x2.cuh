@@ -336,11 +336,22 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
 
   long long tile = blockIdx.x + (long long)gridDim.x * grp;
   Place cur = locate(tile);
-  if (tile < prm.total_tiles) stage(cur);
+  if (grp == 0 && tile < prm.total_tiles) stage(cur);
   // the tables (copied by every thread of the CTA) and this thread's first
   // cp.async copies are complete and visible to all groups
   cp_async_wait_all();
   __syncthreads();
+  // Groups 1 and 2 stage their first tile once the previous group's first
+  // tile has landed, so the first round arrives, and the groups start,
+  // staggered: they do not then run the same phases in lockstep (which
+  // piles all warps of the SM onto the shared-memory pipe at once). A wait
+  // that runs out only ends the stagger; the previous group reports it.
+  if (grp > 0 && tile < prm.total_tiles) {
+    const long long prev = tile - gridDim.x;  // the previous group's first tile
+    if (tid == 0 && locate(prev).tma) mbar_wait_bounded(bar - 1, 0u, nullptr);
+    group_sync(bar_id, THREADS);
+    stage(cur);
+  }
   for (; tile < prm.total_tiles; tile += (long long)gridDim.x * kX2Groups) {
     cp_async_wait_all();
     bool failed = false;
