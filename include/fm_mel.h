@@ -140,6 +140,43 @@ fm_status fm_mel_forward_host(const fm_plan* plan, const void* h_in, int64_t B, 
                               void* h_out, void* d_in_scratch, void* d_out_scratch,
                               fm_stream_t stream);
 
+/* Size in bytes of the device staging array behind
+ * fm_mel_forward_host_noalloc (32 MiB). */
+#define FM_NOALLOC_MAX_BYTES ((size_t)32 << 20)
+
+/*
+ * fm_mel_forward_host_noalloc -- fm_mel_forward_host without caller-supplied
+ * device buffers. The pages have no counterpart: this entry point is for
+ * callers that hold audio in host memory but cannot allocate device memory
+ * when they need a spectrogram -- a real-time audio callback, where
+ * cudaMalloc's implicit device synchronisation and unbounded latency would
+ * miss the deadline, or a process whose device memory is owned by another
+ * framework's allocator.
+ *
+ * Queues on `stream`: a copy of h_in [B][T] (plan's in_dtype) into a staging
+ * array in device memory, the kernel, and a copy of the spectrogram into
+ * h_out [B][n_mels][n_frames] (plan's out_dtype). The staging array is a
+ * static device array of FM_NOALLOC_MAX_BYTES that every GPU loading this
+ * library holds until the process exits; the call allocates nothing.
+ *
+ * Limit: the input bytes, rounded up to 256, plus the output bytes must fit
+ * in FM_NOALLOC_MAX_BYTES (the B = 8 x 480000 f32 speech batch with 128 mels,
+ * 27.7 MB, does); larger calls return FM_ERR_INVALID_ARG before any CUDA work.
+ * Sharing: every call on a device uses the same array and the array keeps the
+ * last call's contents. Calls queued on one stream run in order and are safe;
+ * calls that overlap on the GPU (other streams, other host threads, or two
+ * plans on one device) race on the array and must be serialised by the caller.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, which may make the CUDA runtime load this library's
+ * module on that device); make that first call before any stream capture.
+ * The caller synchronises `stream` before reading h_out; pinned host memory
+ * makes the copies asynchronous.
+ * Errors: as fm_mel_forward_host, plus FM_ERR_INVALID_ARG for sizes beyond
+ * the limit and FM_ERR_CUDA if the address look-up fails.
+ */
+fm_status fm_mel_forward_host_noalloc(const fm_plan* plan, const void* h_in, int64_t B, int64_t T,
+                                      void* h_out, fm_stream_t stream);
+
 /*
  * fm_mel_filterbank_csr -- the plan's filterbank, computed on the host only
  * (no CUDA call), for inspection and tests.

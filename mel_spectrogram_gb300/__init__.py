@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     fm_mel_filterbank_csr,
     fm_mel_forward,
     fm_mel_forward_host,
+    fm_mel_forward_host_noalloc,
     fm_n_frames,
     fm_plan_create,
     fm_plan_destroy,

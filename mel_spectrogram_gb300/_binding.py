@@ -24,6 +24,7 @@ EXPORTS = [
     "fm_n_frames",
     "fm_mel_forward",
     "fm_mel_forward_host",
+    "fm_mel_forward_host_noalloc",
     "fm_mel_filterbank_csr",
     "fm_plan_get_info",
     "fm_plan_poll_error",
@@ -71,6 +72,8 @@ def lib() -> C.CDLL:
     L.fm_mel_forward.restype = ci
     L.fm_mel_forward_host.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
     L.fm_mel_forward_host.restype = ci
+    L.fm_mel_forward_host_noalloc.argtypes = [vp, vp, i64, i64, vp, vp]
+    L.fm_mel_forward_host_noalloc.restype = ci
     L.fm_mel_filterbank_csr.argtypes = [ci, ci, ci, cd, cd, ci, ci, vp, vp, vp, vp, C.POINTER(i64)]
     L.fm_mel_filterbank_csr.restype = ci
     L.fm_plan_get_info.argtypes = [vp, C.POINTER(fm_plan_info)]
@@ -126,6 +129,26 @@ def fm_mel_forward(plan, d_in: int, B: int, T: int, d_out: int, stream: int = 0)
 def fm_mel_forward_host(plan, h_in: int, B: int, T: int, h_out: int, d_in: int, d_out: int, stream: int = 0):
     _check(lib().fm_mel_forward_host(plan, h_in, int(B), int(T), h_out, d_in, d_out, stream or None),
            "fm_mel_forward_host")
+
+
+# size of the device staging array of fm_mel_forward_host_noalloc (FM_NOALLOC_MAX_BYTES)
+FM_NOALLOC_MAX_BYTES = 32 << 20
+
+
+def fm_mel_forward_host_noalloc(plan, h_in: int, B: int, T: int, h_out: int, stream: int = 0) -> None:
+    """Host buffers in and out, device staging in the library's static array.
+
+    For callers that cannot allocate device memory at call time (a real-time
+    audio callback, or a process whose device memory belongs to another
+    allocator). The input bytes (rounded up to 256) plus the output bytes must
+    fit in FM_NOALLOC_MAX_BYTES; calls that overlap on the GPU share the array
+    and race, so queue them on one stream.
+    """
+    st = lib().fm_mel_forward_host_noalloc(plan, h_in, int(B), int(T), h_out, stream or None)
+    if st == FM_ERR_INVALID_ARG:
+        raise FmError(st, "fm_mel_forward_host_noalloc (a NULL buffer, T <= n_fft/2, or input + output beyond "
+                          f"the {FM_NOALLOC_MAX_BYTES}-byte staging array)")
+    _check(st, "fm_mel_forward_host_noalloc")
 
 
 def fm_plan_get_info(plan) -> dict:
