@@ -147,13 +147,62 @@ struct FirstFactor {
   static constexpr int value = (L % 4 == 0) ? 4 : (L % 2 == 0) ? 2 : (L % 5 == 0) ? 5 : (L % 3 == 0) ? 3 : 0;
 };
 
-// L-point DFT by decimation in time, L = R * L2: n = R n2 + n1, k = k2 + L2 k1.
+// Coprime split L = R * L2 for the prime-factor (Good-Thomas) algorithm: R is
+// the power-of-two part of L, L2 the odd part; R = 0 when either is 1.
+template <int L>
+struct CoprimeSplit {
+  static constexpr int pow2 = L & -L;
+  static constexpr int R = (pow2 > 1 && pow2 < L) ? pow2 : 0;
+  static constexpr int L2 = R ? L / R : 0;
+};
+
+// a^-1 mod m for coprime a, m (m small; evaluated by the compiler)
+constexpr int cx_mod_inverse(int a, int m) {
+  for (int x = 1; x < m; ++x)
+    if ((a * x) % m == 1) return x;
+  return m == 1 ? 0 : -1;
+}
+
+template <int L>
+__device__ __forceinline__ void dft(float2 (&x)[L]);
+
+// Prime-factor DFT for coprime L = R * L2 (Good-Thomas): with the input map
+// n = (L2 n1 + R n2) mod L and the Chinese-remainder output map
+// k = (L2 (L2^-1 mod R) k1 + R (R^-1 mod L2) k2) mod L, the kernel W_L^{nk}
+// factors into W_R^{n1 k1} W_L2^{n2 k2}: L2-point DFTs over n2, then R-point
+// DFTs over n1, and no twiddle multiplies between them.
+template <int L, int R, int L2>
+__device__ __forceinline__ void dft_pfa(float2 (&x)[L]) {
+  constexpr int ka = L2 * cx_mod_inverse(L2 % R, R) % L, kb = R * cx_mod_inverse(R % L2, L2) % L;
+  float2 y[R][L2];
+#pragma unroll
+  for (int n1 = 0; n1 < R; ++n1)
+#pragma unroll
+    for (int n2 = 0; n2 < L2; ++n2) y[n1][n2] = x[(L2 * n1 + R * n2) % L];
+#pragma unroll
+  for (int n1 = 0; n1 < R; ++n1) dft<L2>(y[n1]);
+#pragma unroll
+  for (int k2 = 0; k2 < L2; ++k2) {
+    float2 t[R];
+#pragma unroll
+    for (int n1 = 0; n1 < R; ++n1) t[n1] = y[n1][k2];
+    dft<R>(t);
+#pragma unroll
+    for (int k1 = 0; k1 < R; ++k1) x[(ka * k1 + kb * k2) % L] = t[k1];
+  }
+}
+
+// L-point DFT: radix-2/3/4/5 butterflies; the prime-factor split when L has
+// coprime power-of-two and odd parts; otherwise decimation in time,
+// L = R * L2: n = R n2 + n1, k = k2 + L2 k1.
 template <int L>
 __device__ __forceinline__ void dft(float2 (&x)[L]) {
   if constexpr (L == 1) {
     return;
   } else if constexpr (L == 2 || L == 3 || L == 4 || L == 5) {
     butterfly<L>(x);
+  } else if constexpr (CoprimeSplit<L>::R != 0) {
+    dft_pfa<L, CoprimeSplit<L>::R, CoprimeSplit<L>::L2>(x);
   } else {
     constexpr int R = FirstFactor<L>::value;
     static_assert(R != 0, "DFT size must factor into 2, 3, 4 and 5");

@@ -109,13 +109,43 @@ __device__ __forceinline__ void butterfly<5>(cx2 (&a)[5]) {
   a[3] = add_pi(t2, u2);
 }
 
-// L-point DFT by decimation in time, L = R * L2: n = R n2 + n1, k = k2 + L2 k1.
+template <int L>
+__device__ __forceinline__ void dft(cx2 (&x)[L]);
+
+// Prime-factor DFT for coprime L = R * L2, as the float2 version in
+// fm_fft.cuh: no twiddle multiplies between the two stages.
+template <int L, int R, int L2>
+__device__ __forceinline__ void dft_pfa(cx2 (&x)[L]) {
+  constexpr int ka = L2 * cx_mod_inverse(L2 % R, R) % L, kb = R * cx_mod_inverse(R % L2, L2) % L;
+  cx2 y[R][L2];
+#pragma unroll
+  for (int n1 = 0; n1 < R; ++n1)
+#pragma unroll
+    for (int n2 = 0; n2 < L2; ++n2) y[n1][n2] = x[(L2 * n1 + R * n2) % L];
+#pragma unroll
+  for (int n1 = 0; n1 < R; ++n1) dft<L2>(y[n1]);
+#pragma unroll
+  for (int k2 = 0; k2 < L2; ++k2) {
+    cx2 t[R];
+#pragma unroll
+    for (int n1 = 0; n1 < R; ++n1) t[n1] = y[n1][k2];
+    dft<R>(t);
+#pragma unroll
+    for (int k1 = 0; k1 < R; ++k1) x[(ka * k1 + kb * k2) % L] = t[k1];
+  }
+}
+
+// L-point DFT: butterflies, the prime-factor split for coprime power-of-two
+// and odd parts, otherwise decimation in time, L = R * L2: n = R n2 + n1,
+// k = k2 + L2 k1.
 template <int L>
 __device__ __forceinline__ void dft(cx2 (&x)[L]) {
   if constexpr (L == 1) {
     return;
   } else if constexpr (L == 2 || L == 3 || L == 4 || L == 5) {
     butterfly<L>(x);
+  } else if constexpr (CoprimeSplit<L>::R != 0) {
+    dft_pfa<L, CoprimeSplit<L>::R, CoprimeSplit<L>::L2>(x);
   } else {
     constexpr int R = FirstFactor<L>::value;
     static_assert(R != 0, "DFT size must factor into 2, 3, 4 and 5");
