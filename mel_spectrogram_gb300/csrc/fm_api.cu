@@ -162,7 +162,8 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   }
   const int nnz = (int)mw.size();
   X2Schedule x2s;
-  const int x2_warps = var->threads / 32 / fm::kX2Groups;  // warps per tile group of the packed kernel
+  // warps per tile group of the packed kernel (its CTA adds the producer warp)
+  const int x2_warps = (var->threads / 32 - fm::kX2ProducerWarps) / fm::kX2Groups;
   if (var->kind == 1) x2s = build_x2_schedule(n_fft / 2, n_mels, x2_warps, ms, ml, mo, mw);
   const int x2_slots = var->kind == 1 ? x2s.warp_begin.back() : 0;
 

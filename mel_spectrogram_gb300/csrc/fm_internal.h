@@ -84,6 +84,7 @@ constexpr int kX2MaxMels = 256;
 constexpr int kX2MaxWarps = 16;
 constexpr int kX2Unroll = 4;    // chunks per unrolled mel iteration
 constexpr int kX2Groups = 3;    // independent tile groups per CTA (one CTA per SM)
+constexpr int kX2ProducerWarps = 1;  // the warp that stages every group's tiles
 constexpr int kX2MaxSlots = 1024;  // mel chunk slots (4 chunks each) over all warps
 struct X2Tables {
   float4 p1[kX2MaxM];        // as KernelParams::p1
@@ -125,8 +126,9 @@ __host__ __device__ inline int in_row_stride_x2(int len, int esize) { return in_
 // needs no separate input buffer (when a tile fits there; otherwise one is
 // appended).
 struct SmemLayoutX2 {
-  // group g's mbarrier at bars + 8 g, its exchange buffer at xbuf + g group_stride
-  // and its staged tile at in_tile + g group_stride
+  // group g's "tile staged" mbarrier at bars + 8 g and its "staging area free"
+  // mbarrier at bars + 8 (groups + g); its exchange buffer at
+  // xbuf + g group_stride and its staged tile at in_tile + g group_stride
   size_t bars, p1, tw_half, tw_full, desc, w4, xbuf, in_tile, in_tile_bytes, group_stride, total;
 };
 
@@ -144,7 +146,7 @@ __host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int k
   const int ns = n_slots > 0 ? n_slots : 1;
   SmemLayoutX2 L;
   size_t o = 0;
-  L.bars = o;      o = align16(o + sizeof(unsigned long long) * groups);
+  L.bars = o;      o = align16(o + sizeof(unsigned long long) * 2 * groups);
   L.p1 = o;        o = align16(o + sizeof(float4) * M);
   L.tw_half = o;   o = align16(o + sizeof(float4) * M);
   L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));

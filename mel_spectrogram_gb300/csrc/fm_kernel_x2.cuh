@@ -88,23 +88,6 @@ __device__ __forceinline__ void pass1_load_x2(const Raw* __restrict__ base, cons
   }
 }
 
-// Pass 1, compute half: Q-point DFT, four-step twiddle W_M^{p k2}, and one
-// 16-byte store {re_a, re_b, im_a, im_b} per output into row g of the
-// exchange buffer at [k2 * P + p].
-template <int P, int Q>
-__device__ __forceinline__ void pass1_finish_x2(cx2 (&z)[Q], const float4* __restrict__ s_twh4, float4* xq_row,
-                                                int p) {
-  const float4* tw = s_twh4 + p * Q;  // this role's W_M^{p k2}, k2 < Q
-  dft<Q>(z);
-  xq_row[p] = make_float4(z[0].re.x, z[0].re.y, z[0].im.x, z[0].im.y);
-#pragma unroll
-  for (int k2 = 1; k2 < Q; ++k2) {
-    const float4 w = tw[k2];
-    const cx2 v = cmul(z[k2], make_float2(w.x, w.y), make_float2(w.z, w.w));
-    xq_row[k2 * P + p] = make_float4(v.re.x, v.re.y, v.im.x, v.im.y);
-  }
-}
-
 __device__ __forceinline__ cx2 load_cx2(const float4* p) {
   const float4 v = *p;
   return {make_float2(v.x, v.y), make_float2(v.z, v.w)};
@@ -248,15 +231,139 @@ __device__ __forceinline__ void mel_project_x2(const unsigned char* s_pw, const 
   }
 }
 
-// The tile loop of one group: group `grp` of the CTA runs virtual tile slot
-// blockIdx.x + gridDim.x * grp, stepping by gridDim.x * kX2Groups, with its
-// own exchange buffer, staged tile, mbarrier and named barrier 1 + grp.
+// Tile k of tile group g of this CTA: groups take the grid's tile slots in
+// turn, so group g runs tiles blockIdx.x + gridDim.x * (g + kX2Groups * k).
+__device__ __forceinline__ long long x2_tile(int g, int k) {
+  return (long long)blockIdx.x + (long long)gridDim.x * (g + (long long)kX2Groups * k);
+}
+
+// Geometry of the staged tile: lines of KH hops (two for a compile-time hop,
+// else one), `rows` lines with a stride of S samples.
+template <int N, int HOP, typename Raw>
+struct X2Staging {
+  static constexpr int KH = HOP > 0 ? 2 : 1;
+  int hop, line, S, rows;
+  __device__ explicit X2Staging(int runtime_hop) {
+    hop = HOP > 0 ? HOP : runtime_hop;
+    line = KH * hop;
+    S = in_row_stride_x2(line, (int)sizeof(Raw));
+    rows = x2_lines(N, hop, KH);
+  }
+};
+
+// The producer warp: stages every tile of the CTA's groups into the group's
+// staging area (the upper half of its exchange buffer). Lines that lie inside
+// the signal arrive by TMA bulk copies, one line per lane, when the signal's
+// lines start on 16-byte boundaries; their bytes are registered on the group's
+// "staged" mbarrier. The other lines (the reflect-padded edges, or every line
+// of an unaligned signal) are gathered by the warp's lanes with cp.async
+// element copies, mirrored about the first / last sample; lines that start
+// past the padded signal are skipped (no valid frame reads them). Lane 0 then
+// arrives on the mbarrier, so its phase completes once both kinds of copies
+// have landed. A group's next tile is staged once the group reports its
+// staging area free (its "free" mbarrier, after pass 2 has read the exchange
+// buffer); the warp serves whichever group is ready first. Waits are bounded:
+// if no group frees its area for ~2^22 polls the warp records
+// FM_ERR_KERNEL_TIMEOUT and stops staging (the waiting groups then time out).
+template <int N, int HOP, typename Raw>
+__device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay,
+                                           int lane) {
+  const X2Staging<N, HOP, Raw> st(prm.hop);
+  const int esize = (int)sizeof(Raw);
+  const Raw* in = static_cast<const Raw*>(prm.in);
+  const long long T = prm.T;
+  const TileSplitter split(prm.tiles_per_signal);
+  unsigned long long* full = reinterpret_cast<unsigned long long*>(smem + lay.bars);
+  unsigned long long* empty = full + kX2Groups;
+  auto stage = [&](int g, long long tile) {
+    long long b;
+    int tt;
+    split(tile, b, tt);
+    const long long gstart = (long long)tt * kX2Frames * st.hop - prm.pad;
+    const Raw* sig = in + b * T;
+    Raw* dst = reinterpret_cast<Raw*>(smem + lay.in_tile + g * lay.group_stride);
+    const long long L = st.line;
+    // lines [r_lo, r_hi) lie inside [0, T); lines from r_end on start past T + pad
+    long long r_lo = gstart >= 0 ? 0 : (-gstart + L - 1) / L;
+    long long r_hi = (T - gstart) / L;
+    long long r_end = (T + prm.pad - gstart + L - 1) / L;
+    r_end = r_end < st.rows ? r_end : st.rows;
+    r_hi = r_hi < r_end ? r_hi : r_end;
+    const bool tma_ok = ((st.line * esize) & 15) == 0 && (reinterpret_cast<uintptr_t>(sig + gstart) & 15) == 0;
+    if (!tma_ok || r_lo >= r_hi) r_lo = r_hi = 0;
+    // the consumers' generic accesses of the area were ordered before this
+    // warp by the "free" mbarrier; order them before the async-proxy writes
+    if (lane == 0) {
+      fence_proxy_async();
+      if (r_hi > r_lo) mbar_expect_tx(full + g, (unsigned)((r_hi - r_lo) * L * esize));
+    }
+    __syncwarp();
+    for (int r = (int)r_lo + lane; r < (int)r_hi; r += 32)
+      tma_load_1d(dst + r * st.S, sig + gstart + r * L, (unsigned)(L * esize), full + g);
+    if (r_lo > 0) stage_tile<Raw, 1>(sig, T, gstart, (int)r_lo, st.line, st.S, dst, 0, lane);
+    const int r_tail = (int)(r_hi > r_lo ? r_hi : r_lo);
+    if (r_end > r_tail)
+      stage_tile<Raw, 1>(sig, T, gstart + r_tail * L, (int)r_end - r_tail, st.line, st.S, dst + r_tail * st.S, 0,
+                         lane);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncwarp();  // every lane's element copies have landed
+    if (lane == 0) mbar_arrive(full + g);
+  };
+  int next_k[kX2Groups];
+  unsigned phase[kX2Groups];
+#pragma unroll
+  for (int g = 0; g < kX2Groups; ++g) {
+    phase[g] = 0u;
+    next_k[g] = 0;
+    if (x2_tile(g, 0) < prm.total_tiles) {
+      stage(g, x2_tile(g, 0));
+      next_k[g] = 1;
+    }
+  }
+  for (int idle = 0;;) {
+    int ready = -1;
+    bool left = false;
+#pragma unroll
+    for (int g = 0; g < kX2Groups; ++g) {
+      if (x2_tile(g, next_k[g]) >= prm.total_tiles) continue;
+      left = true;
+      if (ready < 0 && mbar_test_wait(empty + g, phase[g])) ready = g;
+    }
+    ready = __shfl_sync(0xffffffffu, ready, 0);
+    if (!left) break;
+    if (ready < 0) {
+      if (++idle > (1 << 22)) {
+        if (lane == 0) atomicExch(prm.err, (unsigned)FM_ERR_KERNEL_TIMEOUT);
+        break;
+      }
+      __nanosleep(32);
+      continue;
+    }
+    idle = 0;
+    phase[ready] ^= 1u;
+    stage(ready, x2_tile(ready, next_k[ready]));
+    ++next_k[ready];
+  }
+}
+
+// The tile loop of one group (P x 16 threads on named barrier 1 + grp, its
+// own exchange buffer and staging area). Per tile:
+//   wait for the staged samples (every thread, on the group's mbarrier);
+//   pass 1 in registers (loads, window, Q-point DFT, twiddles);
+//   barrier: every staged sample has been read and the previous tile's mel
+//            phase has finished reading the power tile;
+//   pass-1 stores; barrier; pass 2 (loads, P-point DFTs); barrier: the
+//   exchange buffer is free, so the producer may stage the next tile into
+//   its upper half while the split writes the power tile into the lower half;
+//   split and |X|^p; barrier; mel projection and stores.
+// A warp that finishes its mel work early runs the next tile's pass 1 while
+// the others finish theirs.
 template <int N, int P, int Q, int HOP, typename Raw>
-__device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay,
-                                             int grp) {
+__device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay,
+                                           int grp) {
   constexpr int M = N / 2;
   constexpr int THREADS = P * kX2Lanes;  // per group
-  constexpr int NWARPS = THREADS / 32;
   constexpr int GS4 = M + 1;  // float4 stride between frame pairs in the exchange buffer (odd)
   const float4* s_p1 = reinterpret_cast<const float4*>(smem + lay.p1);
   const float4* s_twh4 = reinterpret_cast<const float4*>(smem + lay.tw_half);
@@ -266,6 +373,8 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   unsigned char* s_x = smem + lay.xbuf + grp * lay.group_stride;
   float4* s_xq = reinterpret_cast<float4*>(s_x);
   const int bar_id = 1 + grp;
+  unsigned long long* full = reinterpret_cast<unsigned long long*>(smem + lay.bars) + grp;
+  unsigned long long* empty = full + kX2Groups;
 
   const int tid = threadIdx.x - grp * THREADS, warp = tid >> 5, lane = tid & 31;
   const int g = tid % kX2Lanes, role = tid / kX2Lanes;
@@ -274,116 +383,43 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
   // g writes its pair (g, g + 16) at float2 slot 2 (g % 8) + g / 8.
   const unsigned char* s_pw = s_x;
   float2* pw_col = reinterpret_cast<float2*>(s_x) + 2 * (g & 7) + (g >> 3);
-  const int esize = (int)sizeof(Raw);
-  constexpr int KH = HOP > 0 ? 2 : 1;  // hops per staged line
-  const int hop = HOP > 0 ? HOP : prm.hop, line = KH * hop;
-  const int S = in_row_stride_x2(line, esize), rows = x2_lines(N, hop, KH);
-  const Raw* in = static_cast<const Raw*>(prm.in);
-  const long long T = prm.T;
+  const X2Staging<N, HOP, Raw> st(prm.hop);
   const TileSplitter split(prm.tiles_per_signal);
   const int s_begin = __ldg(&prm.x2->warp_begin[warp]), s_end = __ldg(&prm.x2->warp_begin[warp + 1]);
-  unsigned long long* bar = reinterpret_cast<unsigned long long*>(smem + lay.bars) + grp;
-  // Where a tile lives: signal b, tile index tt within it, signal index of
-  // tile position 0, and whether it is interior with 16-byte aligned rows
-  // (then TMA bulk copies stage it). Computed once per tile and carried.
-  struct Place {
-    long long b;
-    int tt;
-    bool tma;
-  };
-  auto first_sample = [&](const Place& pl) { return (long long)pl.tt * kX2Frames * hop - prm.pad; };
-  auto locate = [&](long long tile) {
-    Place pl;
-    split(tile, pl.b, pl.tt);
-    const long long gstart = first_sample(pl);
-    const Raw* src = in + pl.b * T;
-    pl.tma = gstart >= 0 && gstart + (long long)rows * line <= T && ((hop * esize) & 15) == 0 &&
-             (reinterpret_cast<uintptr_t>(src + gstart) & 15) == 0;
-    return pl;
-  };
-  // Stage a tile into the input area: TMA row copies issued by one lane of
-  // every warp (rows dealt round robin) completing on the mbarrier, or
-  // cp.async element copies by all threads at the signal edges. The area was
-  // last written through the generic proxy (exchange stores), hence the proxy
-  // fence before each issuing lane's first copy.
-  Raw* s_in = reinterpret_cast<Raw*>(smem + lay.in_tile + grp * lay.group_stride);
+  const Raw* s_in = reinterpret_cast<const Raw*>(smem + lay.in_tile + grp * lay.group_stride);
   // frame g's first sample (HOP > 0: plus 2p, the role's first pair)
-  const Raw* fbase = HOP > 0 ? s_in + (g >> 1) * S + (g & 1) * hop + 2 * role : s_in + g * S;
-  const Raw* fbase_o = fbase + ((HOP > 0 && (g & 1)) ? S - line : 0);
-  auto stage = [&](const Place& pl) {
-    const Raw* src = in + pl.b * T + first_sample(pl);
-    if (pl.tma) {
-      // The barrier's single arrival carries the byte count, so its phase
-      // cannot complete before it even if some copies land first.
-      if (tid == 0) mbar_arrive_expect_tx(bar, (unsigned)(rows * line * esize));
-      if (lane == 0) {
-        fence_proxy_async();
-        for (int r = warp; r < rows; r += NWARPS)
-          tma_load_1d(s_in + r * S, src + (long long)r * line, (unsigned)(line * esize), bar);
-      }
-    } else {
-      stage_tile<Raw, NWARPS>(in + pl.b * T, T, first_sample(pl), rows, line, S, s_in, warp, lane);
-    }
-    cp_async_commit();
-  };
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();  // the barriers exist before anyone polls them
-  pdl_wait();       // caller buffers only after the previous kernel in the stream is done
+  const Raw* fbase = HOP > 0 ? s_in + (g >> 1) * st.S + (g & 1) * st.hop + 2 * role : s_in + g * st.S;
+  const Raw* fbase_o = fbase + ((HOP > 0 && (g & 1)) ? st.S - st.line : 0);
+  float4* xq_row = s_xq + g * GS4;
+  const float4* tw = s_twh4 + role * Q;  // this role's W_M^{p k2}, k2 < Q
   unsigned phase = 0u;
 
-  long long tile = blockIdx.x + (long long)gridDim.x * grp;
-  Place cur = locate(tile);
-  if (grp == 0 && tile < prm.total_tiles) stage(cur);
-  // the tables (copied by every thread of the CTA) and this thread's first
-  // cp.async copies are complete and visible to all groups
-  cp_async_wait_all();
-  __syncthreads();
-  // Groups 1 and 2 stage their first tile once the previous group's first
-  // tile has landed, so the first round arrives, and the groups start,
-  // staggered: they do not then run the same phases in lockstep (which
-  // piles all warps of the SM onto the shared-memory pipe at once). A wait
-  // that runs out only ends the stagger; the previous group reports it.
-  if (grp > 0 && tile < prm.total_tiles) {
-    const long long prev = tile - gridDim.x;  // the previous group's first tile
-    if (tid == 0 && locate(prev).tma) mbar_wait_bounded(bar - 1, 0u, nullptr);
-    group_sync(bar_id, THREADS);
-    stage(cur);
-  }
-  for (; tile < prm.total_tiles; tile += (long long)gridDim.x * kX2Groups) {
-    cp_async_wait_all();
-    bool failed = false;
-    if (cur.tma) {
-      // one thread waits for the copies; the barrier below then orders them
-      // for the whole group while the other warps sleep instead of polling
-      if (tid == 0) failed = !mbar_wait_bounded(bar, phase, prm.err);
-      phase ^= 1u;
-    }
-    // this tile's samples are visible; the previous tile's mel phase is done
-    if (group_sync_or(bar_id, THREADS, failed)) return;  // a staging copy never arrived (error recorded)
+  for (int k = 0;; ++k) {
+    const long long tile = x2_tile(grp, k);
+    if (tile >= prm.total_tiles) break;
+    const bool ok = mbar_wait_bounded(full, phase, prm.err);
+    phase ^= 1u;
 
-    float4* xq_row = s_xq + g * GS4;
     cx2 z[Q];
-    pass1_load_x2<P, Q, HOP, Raw>(fbase, fbase_o, S, s_p1, role, z);
-    group_sync(bar_id, THREADS);  // samples are in registers: the exchange buffer (holding them) may be overwritten
-    pass1_finish_x2<P, Q>(z, s_twh4, xq_row, role);
+    pass1_load_x2<P, Q, HOP, Raw>(fbase, fbase_o, st.S, s_p1, role, z);
+    dft<Q>(z);
+#pragma unroll
+    for (int k2 = 1; k2 < Q; ++k2) {
+      const float4 w = tw[k2];
+      z[k2] = cmul(z[k2], make_float2(w.x, w.y), make_float2(w.z, w.w));
+    }
+    // staged samples all read, previous power tile no longer needed
+    if (group_sync_or(bar_id, THREADS, !ok)) return;  // staging never arrived (error recorded)
+#pragma unroll
+    for (int k2 = 0; k2 < Q; ++k2) xq_row[k2 * P + role] = make_float4(z[k2].re.x, z[k2].re.y, z[k2].im.x, z[k2].im.y);
     group_sync(bar_id, THREADS);
 
     cx2 za[P], zb[P];
     pass2_x2<P, Q>(xq_row, role, za, zb);
-    group_sync(bar_id, THREADS);  // exchange reads done: power tile (lower half) and next tile (upper half) may land
-    // this tile's output place; then the next tile starts landing during the
-    // split and the mel projection
-    const int t0 = cur.tt * kX2Frames;
-    const int n_valid = min(kX2Frames, prm.n_frames - t0);
-    const long long obase = cur.b * prm.n_mels * (long long)prm.n_frames + t0;
-    const long long next = tile + (long long)gridDim.x * kX2Groups;
-    cur = Place{};
-    if (next < prm.total_tiles) {
-      cur = locate(next);
-      stage(cur);
+    group_sync(bar_id, THREADS);  // exchange reads done
+    if (tid == 0) {
+      fence_proxy_async();  // the group's generic accesses before the producer's TMA writes
+      mbar_arrive(empty);   // the staging area (upper half) is free for the next tile
     }
     const bool merged = role < 2;  // the warp that holds role 0 (and role 1)
     switch (prm.power_mode) {
@@ -393,6 +429,12 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
     }
     group_sync(bar_id, THREADS);
 
+    long long b;
+    int tt;
+    split(tile, b, tt);
+    const int t0 = tt * kX2Frames;
+    const int n_valid = min(kX2Frames, prm.n_frames - t0);
+    const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
     if (prm.out_dtype == FM_F32)
       mel_project_x2(s_pw, s_desc, s_w4, static_cast<float*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
                      s_end, lane);
@@ -400,47 +442,64 @@ __device__ __forceinline__ void run_tiles_x2(const KernelParams& prm, unsigned c
       mel_project_x2(s_pw, s_desc, s_w4, static_cast<__half*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
                      s_end, lane);
   }
-  cp_async_commit();  // nothing may stay in flight past the end of the CTA
-  cp_async_wait_all();
 }
 
-// One CTA per SM: kX2Groups groups of P x 16 threads, each running its own
-// tile loop on its own exchange buffer; the tables are shared.
+// One CTA per SM: kX2Groups tile groups of P x 16 threads, each running its
+// own tile loop on its own exchange buffer, and one producer warp that stages
+// all their tiles; the tables are shared.
 template <int N, int P, int Q, int HOP>
-__global__ void __launch_bounds__(kX2Groups* P* kX2Lanes, 1) mel_kernel_x2(const KernelParams prm) {
+__global__ void __launch_bounds__(kX2Groups* P* kX2Lanes + 32 * kX2ProducerWarps, 1)
+    mel_kernel_x2(const KernelParams prm) {
   constexpr int M = N / 2;
   constexpr int GROUP = P * kX2Lanes;
-  constexpr int THREADS = kX2Groups * GROUP;
+  constexpr int CONSUMERS = kX2Groups * GROUP;
   static_assert(P * Q == M && Q == 2 * P && M <= kX2MaxM, "x2 kernel needs Q = 2P and M <= 200");
   static_assert(GROUP % 32 == 0, "a group must be whole warps");
+  static_assert(kX2ProducerWarps == 1, "one producer warp");
   extern __shared__ __align__(16) unsigned char smem[];
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
   const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, HOP > 0 ? 2 : 1, prm.x2_slots, esize, kX2Groups);
   pdl_launch_dependents();
-  // tables, fetched once per CTA; every thread waits for its copies before
-  // the CTA-wide barrier that precedes the tile loops
   const int tid = threadIdx.x;
-  const X2Tables* t = prm.x2;
-  copy_table_async(smem + lay.p1, t->p1, (int)sizeof(float4) * M, tid, THREADS);
-  copy_table_async(smem + lay.tw_half, t->tw_half, (int)sizeof(float4) * M, tid, THREADS);
-  copy_table_async(smem + lay.tw_full, t->tw_full, (int)sizeof(float4) * (M + 1), tid, THREADS);
-  copy_table_async(smem + lay.desc, t->desc, (int)sizeof(int2) * 4 * prm.x2_slots, tid, THREADS);
-  copy_table_async(smem + lay.w4, t->w4, (int)sizeof(float4) * 4 * prm.x2_slots, tid, THREADS);
+  if (tid == CONSUMERS) {
+    unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + lay.bars);
+    for (int i = 0; i < 2 * kX2Groups; ++i) mbar_init(bars + i, 1);
+    fence_mbar_init();
+  }
+  // tables, fetched once per CTA by the consumer threads
+  if (tid < CONSUMERS) {
+    const X2Tables* t = prm.x2;
+    copy_table_async(smem + lay.p1, t->p1, (int)sizeof(float4) * M, tid, CONSUMERS);
+    copy_table_async(smem + lay.tw_half, t->tw_half, (int)sizeof(float4) * M, tid, CONSUMERS);
+    copy_table_async(smem + lay.tw_full, t->tw_full, (int)sizeof(float4) * (M + 1), tid, CONSUMERS);
+    copy_table_async(smem + lay.desc, t->desc, (int)sizeof(int2) * 4 * prm.x2_slots, tid, CONSUMERS);
+    copy_table_async(smem + lay.w4, t->w4, (int)sizeof(float4) * 4 * prm.x2_slots, tid, CONSUMERS);
+  }
+  pdl_wait();       // caller buffers only after the previous kernel in the stream is done
+  __syncthreads();  // the mbarriers exist before anyone uses them
+  if (tid >= CONSUMERS) {
+    if (prm.in_dtype == FM_F32) produce_x2<N, HOP, float>(prm, smem, lay, tid & 31);
+    else if (prm.in_dtype == FM_I16) produce_x2<N, HOP, short>(prm, smem, lay, tid & 31);
+    else produce_x2<N, HOP, __half>(prm, smem, lay, tid & 31);
+    return;
+  }
+  cp_async_wait_all();
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + kX2Groups), "r"(CONSUMERS) : "memory");  // tables visible
   // warp-uniform (a group is whole warps); reading it through a shuffle lets
   // the compiler keep the group's base addresses in uniform registers
   const int grp = __shfl_sync(0xffffffffu, tid / GROUP, 0);
-  if (prm.in_dtype == FM_F32) run_tiles_x2<N, P, Q, HOP, float>(prm, smem, lay, grp);
-  else if (prm.in_dtype == FM_I16) run_tiles_x2<N, P, Q, HOP, short>(prm, smem, lay, grp);
-  else run_tiles_x2<N, P, Q, HOP, __half>(prm, smem, lay, grp);
+  if (prm.in_dtype == FM_F32) consume_x2<N, P, Q, HOP, float>(prm, smem, lay, grp);
+  else if (prm.in_dtype == FM_I16) consume_x2<N, P, Q, HOP, short>(prm, smem, lay, grp);
+  else consume_x2<N, P, Q, HOP, __half>(prm, smem, lay, grp);
 }
 
 }  // namespace fm
 
 // Instantiate one two-frames-per-thread variant:
 // FM_DEFINE_VARIANT_X2(name, N, P, Q, HOP) with HOP = 0 for any hop
-#define FM_DEFINE_VARIANT_X2(NAME, N, P, Q, HOP)                                              \
-  namespace fm {                                                                              \
-  template __global__ void mel_kernel_x2<N, P, Q, HOP>(const KernelParams);                  \
-  extern const Variant NAME = {N, P, Q, kX2Frames, kX2Groups * P * kX2Lanes, 2, 1,             \
-                               (const void*)&mel_kernel_x2<N, P, Q, HOP>, HOP};               \
+#define FM_DEFINE_VARIANT_X2(NAME, N, P, Q, HOP)                                                       \
+  namespace fm {                                                                                       \
+  template __global__ void mel_kernel_x2<N, P, Q, HOP>(const KernelParams);                           \
+  extern const Variant NAME = {N,  P, Q, kX2Frames, kX2Groups * P * kX2Lanes + 32 * kX2ProducerWarps, \
+                               2,  1, (const void*)&mel_kernel_x2<N, P, Q, HOP>, HOP};                \
   }
