@@ -10,6 +10,8 @@
 #include <new>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
 #include "fm_host.h"
 #include "fm_internal.h"
 #include "fm_mel.h"
@@ -120,6 +122,59 @@ X2Schedule build_x2_schedule(int M, int n_mels, int n_warps, const std::vector<i
     S.warp_begin.push_back(S.warp_begin.back() + (int)len);
   }
   return S;
+}
+
+// cuTensorMapEncodeTiled from the driver, resolved once through the runtime
+// (no link against libcuda); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// The packed kernel's tensor map over the input (see KernelParams::tmap):
+// per signal, rows of one staged line starting at the sample where tile rows
+// start (-pad mod line), each row wholly inside the signal; the box is a
+// whole staged tile at the padded pitch. Left unset (tmap_ok = 0) when the
+// layout does not allow it; the kernel then copies line by line.
+void encode_input_map(const fm_plan* plan, const void* d_in, int64_t B, int64_t T, fm::KernelParams& prm) {
+  prm.tmap_ok = 0;
+  prm.tmap_off = 0;
+  prm.tmap_rows = 0;
+  const fm::Variant* v = plan->var;
+  if (v->kind != 1) return;
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return;
+  const int64_t esize = dtype_size(plan->in_dtype);
+  const int kh = v->hop > 0 ? 2 : 1;
+  const int64_t line = (int64_t)kh * plan->hop;
+  const int64_t pitch = (int64_t)fm::in_row_stride_x2((int)line, (int)esize) * esize;  // bytes per staged row
+  const int64_t rows = fm::x2_lines(plan->n_fft, plan->hop, kh);
+  const int64_t pad = plan->n_fft / 2;
+  const int64_t off = ((-pad) % line + line) % line;
+  const uintptr_t base = reinterpret_cast<uintptr_t>(d_in) + (uintptr_t)(off * esize);
+  if ((line * esize) % 16 != 0 || (T * esize) % 16 != 0 || base % 16 != 0) return;
+  if (pitch / 8 > 256 || rows > 256 || B > ((int64_t)1 << 31) || T - off < line) return;
+  const int64_t per_signal = (T - off) / line;
+  if (per_signal > ((int64_t)1 << 31)) return;
+  const cuuint64_t dims[3] = {(cuuint64_t)(line * esize / 8), (cuuint64_t)per_signal, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)(line * esize), (cuuint64_t)(T * esize)};
+  const cuuint32_t box[3] = {(cuuint32_t)(pitch / 8), (cuuint32_t)rows, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  if (encode(&prm.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, reinterpret_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return;
+  prm.tmap_ok = 1;
+  prm.tmap_off = (int)off;
+  prm.tmap_rows = (int)per_signal;
 }
 
 fm_status from_cuda(cudaError_t e) {
@@ -361,6 +416,7 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
 
   const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
   prm.x2 = plan->x2;
+  encode_input_map(plan, d_in, B, T, prm);
   void* args[] = {&prm};
   // programmatic dependent launch: the kernel waits (griddepcontrol.wait) for
   // the previous kernel in the stream before it reads d_in or writes d_out, so

@@ -1,6 +1,7 @@
 // Internal declarations shared by the C-ABI layer and the sm_103a kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,6 +42,14 @@ struct KernelParams {
   const struct X2Tables* x2;  // two-frames-per-thread kernel only
   int x2_slots;               // its mel chunk slots (X2Tables::desc rows in use)
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
+  // Packed kernel: when tmap_ok, every signal is described to the TMA unit as
+  // rows of one staged line (line * in_bytes / 8 elements of 8 bytes) that
+  // start at sample tmap_off + y * line, tmap_rows rows per signal, and the
+  // box is one whole staged tile at its padded row pitch (the pad columns lie
+  // outside the rows and arrive zero-filled). An interior tile is then one
+  // tensor copy.
+  CUtensorMap tmap;  // 128-byte aligned by its type
+  int tmap_ok, tmap_off, tmap_rows;
 };
 
 // Row stride (elements) of the staged input tile: rows hold `hop` samples; a
@@ -53,6 +62,7 @@ __host__ __device__ inline int in_rows(int n_fft, int hop, int frames_per_tile) 
 }
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+__host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
 
 // Dynamic shared-memory layout of one CTA, in bytes from the base.
 struct SmemLayout {
@@ -152,11 +162,13 @@ __host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int k
   L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));
   L.desc = o;      o = align16(o + sizeof(int2) * 4 * ns);
   L.w4 = o;        o = align16(o + sizeof(float4) * 4 * ns);
-  const size_t xq_bytes = align16(sizeof(float4) * 16 * (size_t)(M + 1));
-  const size_t half = align16(xq_bytes / 2);  // >= the power tile, (M + 1) bins x 16 lanes x float2
+  // staging areas start on 128-byte boundaries (tensor TMA destinations)
+  const size_t xq_bytes = align128(sizeof(float4) * 16 * (size_t)(M + 1));
+  const size_t half = align128(xq_bytes / 2);  // >= the power tile, (M + 1) bins x 16 lanes x float2
+  o = align128(o);
   L.xbuf = o;
   L.in_tile_bytes =
-      align16((size_t)in_esize * x2_lines(n_fft, hop, k_hops) * in_row_stride_x2(k_hops * hop, in_esize));
+      align128((size_t)in_esize * x2_lines(n_fft, hop, k_hops) * in_row_stride_x2(k_hops * hop, in_esize));
   if (L.in_tile_bytes <= xq_bytes - half) {
     L.in_tile = L.xbuf + half;
     L.group_stride = xq_bytes;

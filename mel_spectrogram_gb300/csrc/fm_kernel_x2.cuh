@@ -291,11 +291,21 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     r_hi = r_hi < r_end ? r_hi : r_end;
     const bool tma_ok = ((st.line * esize) & 15) == 0 && (reinterpret_cast<uintptr_t>(sig + gstart) & 15) == 0;
     if (!tma_ok || r_lo >= r_hi) r_lo = r_hi = 0;
+    // an interior tile whose rows all lie in the tensor map: one tensor copy
+    const long long y0 = (gstart - prm.tmap_off) / L;
+    const bool one_copy = prm.tmap_ok && gstart >= prm.tmap_off && y0 + st.rows <= prm.tmap_rows &&
+                          (smem_addr(dst) & 127u) == 0;
+    if (one_copy) r_lo = r_hi = r_end = 0;
     // the consumers' generic accesses of the area were ordered before this
     // warp by the "free" mbarrier; order them before the async-proxy writes
     if (lane == 0) {
       fence_proxy_async();
-      if (r_hi > r_lo) mbar_expect_tx(full + g, (unsigned)((r_hi - r_lo) * L * esize));
+      if (one_copy) {
+        mbar_expect_tx(full + g, (unsigned)(st.rows * st.S * esize));
+        tma_load_3d(dst, &prm.tmap, 0, (int)y0, (int)b, full + g);
+      } else if (r_hi > r_lo) {
+        mbar_expect_tx(full + g, (unsigned)((r_hi - r_lo) * L * esize));
+      }
     }
     __syncwarp();
     for (int r = (int)r_lo + lane; r < (int)r_hi; r += 32)
@@ -449,14 +459,14 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
 // all their tiles; the tables are shared.
 template <int N, int P, int Q, int HOP>
 __global__ void __launch_bounds__(kX2Groups* P* kX2Lanes + 32 * kX2ProducerWarps, 1)
-    mel_kernel_x2(const KernelParams prm) {
+    mel_kernel_x2(const __grid_constant__ KernelParams prm) {
   constexpr int M = N / 2;
   constexpr int GROUP = P * kX2Lanes;
   constexpr int CONSUMERS = kX2Groups * GROUP;
   static_assert(P * Q == M && Q == 2 * P && M <= kX2MaxM, "x2 kernel needs Q = 2P and M <= 200");
   static_assert(GROUP % 32 == 0, "a group must be whole warps");
   static_assert(kX2ProducerWarps == 1, "one producer warp");
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
   const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, HOP > 0 ? 2 : 1, prm.x2_slots, esize, kX2Groups);
   pdl_launch_dependents();
@@ -499,7 +509,7 @@ __global__ void __launch_bounds__(kX2Groups* P* kX2Lanes + 32 * kX2ProducerWarps
 // FM_DEFINE_VARIANT_X2(name, N, P, Q, HOP) with HOP = 0 for any hop
 #define FM_DEFINE_VARIANT_X2(NAME, N, P, Q, HOP)                                                       \
   namespace fm {                                                                                       \
-  template __global__ void mel_kernel_x2<N, P, Q, HOP>(const KernelParams);                           \
+  template __global__ void mel_kernel_x2<N, P, Q, HOP>(const __grid_constant__ KernelParams);        \
   extern const Variant NAME = {N,  P, Q, kX2Frames, kX2Groups * P * kX2Lanes + 32 * kX2ProducerWarps, \
                                2,  1, (const void*)&mel_kernel_x2<N, P, Q, HOP>, HOP};                \
   }
