@@ -17,7 +17,7 @@
 //             into shared memory and read as broadcasts;
 //   pass 1  : two LDS.64 pair loads per step, the window multiply scatters
 //             them into the packed layout; Q-point DFT; twiddle W_M^{p k2};
-//             one 16-byte store {re_a, re_b, im_a, im_b} per value;
+//             {re_a, re_b, im_a, im_b} per value as two 8-byte stores;
 //   pass 2  : P-point DFTs for k2 = t and Q - t (role 0: 0 and Q/2), then the
 //             real-FFT split and |X|^p, still packed;
 //   power   : tile rows P[k] of 32 frames, 16 bytes per 4 frames;
@@ -420,8 +420,15 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
     }
     // staged samples all read, previous power tile no longer needed
     if (group_sync_or(bar_id, THREADS, !ok)) return;  // staging never arrived (error recorded)
+    // {re_a, re_b, im_a, im_b} per value, as two 8-byte stores of the register
+    // pairs the packed math left them in (one 16-byte store would first copy
+    // them into an aligned quad)
 #pragma unroll
-    for (int k2 = 0; k2 < Q; ++k2) xq_row[k2 * P + role] = make_float4(z[k2].re.x, z[k2].re.y, z[k2].im.x, z[k2].im.y);
+    for (int k2 = 0; k2 < Q; ++k2) {
+      float2* dst = reinterpret_cast<float2*>(xq_row + k2 * P + role);
+      dst[0] = z[k2].re;
+      dst[1] = z[k2].im;
+    }
     group_sync(bar_id, THREADS);
 
     cx2 za[P], zb[P];
