@@ -8,14 +8,13 @@
 //             runtime value) in the upper half of the exchange buffer,
 //             which is free from the end of pass 2 (the power tile uses the
 //             lower half) to the start of the next pass 1: the next tile
-//             lands during the split and the mel projection. TMA bulk copies
-//             (one per line, dealt to one lane of every warp, completing on
-//             an mbarrier) for interior tiles with 16-byte aligned lines,
-//             cp.async element copies otherwise. Small shared memory per CTA
-//             (no separate input buffers) fits three CTAs per SM;
+//             lands during the split and the mel projection. A producer
+//             warp stages every group's tiles: one tensor-map TMA copy per
+//             interior tile, line copies plus cp.async element copies at the
+//             signal edges;
 //   tables  : window/offset, twiddles and filters are copied once per CTA
 //             into shared memory and read as broadcasts;
-//   pass 1  : two LDS.64 pair loads per step, the window multiply scatters
+//   pass 1  : two 8-byte pair loads per step, the window multiply scatters
 //             them into the packed layout; Q-point DFT; twiddle W_M^{p k2};
 //             {re_a, re_b, im_a, im_b} per value as two 8-byte stores;
 //   pass 2  : P-point DFTs for k2 = t and Q - t (role 0: 0 and Q/2), then the
