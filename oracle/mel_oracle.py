@@ -13,6 +13,15 @@ helpers ``make_window`` and ``pack_fbank`` in ``flashmel/filters.py``):
     -> n_fft-point real DFT (bins 0..n_fft/2) -> |X|^power
     -> triangular mel filterbank (HTK or Slaney scale, optional Slaney norm)
 
+with the framing options the page lists among the supported torchaudio
+arguments (README "Usage": pad, center, pad_mode, normalized; "How it works":
+padding and all four pad modes applied as index arithmetic, the normalized
+modes folded into the window):
+
+    zero-pad `pad` samples on both sides -> (center) pad n_fft/2 on both
+    sides by pad_mode (reflect / constant / replicate / circular) -> frame
+    -> window scaled by the normalisation -> DFT -> ...
+
 Every step is the plain definition, in float64, in the page's order. The DFT
 is the naive O(N^2) sum written as a matmul against explicit cos/sin
 matrices: no FFT, no blocking, no fusion.
@@ -27,7 +36,14 @@ page only names torchaudio's ``melscale_fbanks``):
     mel(f_min) and mel(f_max); triangles are linear in Hz;
   * Slaney norm scales filter m by 2 / (f[m+2] - f[m]) (unit area);
   * reflect padding mirrors about the edge sample without repeating it;
-  * int16 input is scaled by 1/32768; f16 input widens exactly.
+  * int16 input is scaled by 1/32768; f16 input widens exactly;
+  * the pad modes are torch's: constant fills zeros, replicate repeats the
+    edge sample, circular wraps around the signal; `pad` zero-pads before the
+    centre padding, which then mirrors / repeats / wraps the zero-padded
+    signal; without centring, frames start at sample 0 and there are
+    1 + floor((T - n_fft) / hop) of them;
+  * normalized "window" (or True) divides the spectrum by sqrt(sum w^2),
+    "frame_length" by sqrt(n_fft) (torch.stft's normalisation).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, Parseval, filterbank invariants).
@@ -78,9 +94,53 @@ def reflect_pad(x: np.ndarray, pad: int) -> np.ndarray:
     return np.concatenate([left, x, right], axis=-1)
 
 
+PAD_MODES = ("reflect", "constant", "replicate", "circular")
+
+
+def centre_pad(x: np.ndarray, pad: int, mode: str) -> np.ndarray:
+    """Pad the last axis by ``pad`` on each side by ``mode``.
+
+    Position i of the result holds x[i - pad] inside; outside, with
+    j = i - pad < 0 or j >= T:
+      reflect   : x[-j] / x[2(T-1) - j]   (mirror without the edge; T > pad)
+      replicate : x[0] / x[T-1]
+      circular  : x[j mod T]               (T >= pad)
+      constant  : 0
+    """
+    if mode == "reflect":
+        return reflect_pad(x, pad)
+    T = x.shape[-1]
+    j = np.arange(-pad, T + pad)
+    if mode == "replicate":
+        return x[..., np.clip(j, 0, T - 1)]
+    if mode == "circular":
+        if pad > T:
+            raise ValueError(f"circular padding needs T >= pad (T={T}, pad={pad})")
+        return x[..., j % T]
+    if mode == "constant":
+        out = np.zeros(x.shape[:-1] + (T + 2 * pad,), dtype=x.dtype)
+        out[..., pad : pad + T] = x
+        return out
+    raise ValueError(mode)
+
+
+def zero_pad(x: np.ndarray, pad: int) -> np.ndarray:
+    """torchaudio's ``pad`` argument: ``pad`` zeros on each side of the signal."""
+    if pad == 0:
+        return x
+    return centre_pad(x, pad, "constant")
+
+
 def n_frames(T: int, hop: int) -> int:
     """Frame count with centre padding: 1 + floor(T / hop)."""
     return 1 + T // hop
+
+
+def n_frames_uncentred(T: int, n_fft: int, hop: int) -> int:
+    """Frame count without centre padding: 1 + floor((T - n_fft) / hop)."""
+    if T < n_fft:
+        raise ValueError(f"without centring the signal must hold one frame (T={T}, n_fft={n_fft})")
+    return 1 + (T - n_fft) // hop
 
 
 def frame(xp: np.ndarray, n_fft: int, hop: int, count: int) -> np.ndarray:
@@ -143,16 +203,42 @@ def spectral_power(X: np.ndarray, power: float) -> np.ndarray:
     return mag2 ** (power / 2.0)
 
 
+def window_norm(w: np.ndarray, n_fft: int, normalized) -> float:
+    """Scale folded into the window: 1, 1/sqrt(sum w^2) ("window" or True),
+    or 1/sqrt(n_fft) ("frame_length")."""
+    if normalized in (False, None, "none"):
+        return 1.0
+    if normalized in (True, "window"):
+        return 1.0 / math.sqrt(float(np.sum(w * w)))
+    if normalized == "frame_length":
+        return 1.0 / math.sqrt(n_fft)
+    raise ValueError(normalized)
+
+
 def power_spectrogram(
-    x: np.ndarray, n_fft: int, hop: int, win_length: int | None = None, power: float = 2.0
+    x: np.ndarray,
+    n_fft: int,
+    hop: int,
+    win_length: int | None = None,
+    power: float = 2.0,
+    center: bool = True,
+    pad_mode: str = "reflect",
+    pad: int = 0,
+    normalized=False,
 ) -> np.ndarray:
     """Steps a1-a6 for input [..., T] -> [..., n_fft//2 + 1, n_frames]."""
     win_length = n_fft if win_length is None else win_length
-    xd = to_float64(x)
+    xd = zero_pad(to_float64(x), pad)
     T = xd.shape[-1]
-    xp = reflect_pad(xd, n_fft // 2)
-    frames = frame(xp, n_fft, hop, n_frames(T, hop))
-    y = frames * hann_periodic(win_length, n_fft)
+    if center:
+        xp = centre_pad(xd, n_fft // 2, pad_mode)
+        count = n_frames(T, hop)
+    else:
+        xp = xd
+        count = n_frames_uncentred(T, n_fft, hop)
+    frames = frame(xp, n_fft, hop, count)
+    w = hann_periodic(win_length, n_fft)
+    y = frames * (w * window_norm(w, n_fft, normalized))
     P = spectral_power(dft_onesided(y), power)
     return np.swapaxes(P, -1, -2)
 
@@ -243,8 +329,12 @@ def mel_spectrogram(
     scale: str = "htk",
     norm: str | None = None,
     win_length: int | None = None,
+    center: bool = True,
+    pad_mode: str = "reflect",
+    pad: int = 0,
+    normalized=False,
 ) -> np.ndarray:
     """Input [..., T] (f32 / int16 / f16) -> float64 [..., n_mels, n_frames]."""
-    P = power_spectrogram(x, n_fft, hop, win_length, power)  # [..., n_freqs, n_frames]
+    P = power_spectrogram(x, n_fft, hop, win_length, power, center, pad_mode, pad, normalized)
     F = mel_filterbank(n_fft, sr, n_mels, f_min, f_max, scale, norm)
     return np.einsum("mk,...kt->...mt", F, P)

@@ -4,7 +4,8 @@ Each ``check_*`` takes an oracle module (the real one, or a copy with a planted
 mistake) and raises AssertionError if the module disagrees with something the
 pages or the mathematics fix independently:
 
-  * brute force: an explicit triple loop (mirrored list, complex exponentials);
+  * brute force: an explicit triple loop (mirrored list, complex exponentials),
+    and one that spells out every pad mode, centring, `pad` and normalisation;
   * closed forms: an impulse, and a bin-centre cosine through the whole chain;
   * Parseval's identity for the one-sided DFT;
   * filterbank invariants: mel-equispaced vertices, support, partition of
@@ -63,6 +64,68 @@ def check_brute_force(o):
             got = o.power_spectrogram(x, n_fft, hop, win, p)
             assert got.shape == ref.shape, (got.shape, ref.shape)
             assert np.allclose(got, ref, rtol=1e-10, atol=1e-9), (n_fft, hop, win, T, p)
+
+
+def brute_power_framed(x, n_fft, hop, win_length, power, center, pad_mode, pad, normalized):
+    """Naive STFT power with every framing option spelled out sample by sample."""
+    x = [0.0] * pad + [float(v) for v in x] + [0.0] * pad  # torchaudio `pad`: zeros first
+    T = len(x)
+    c = n_fft // 2 if center else 0
+
+    def sample(i):  # position i of the centre-padded signal
+        j = i - c
+        if 0 <= j < T:
+            return x[j]
+        if pad_mode == "constant":
+            return 0.0
+        if pad_mode == "replicate":
+            return x[0] if j < 0 else x[T - 1]
+        if pad_mode == "circular":
+            return x[j + T] if j < 0 else x[j - T]
+        # reflect: the sample as far inside from the edge as j is outside
+        return x[-j] if j < 0 else x[(T - 1) - (j - (T - 1))]
+
+    lpad = (n_fft - win_length) // 2
+    w = [0.0] * n_fft
+    for n in range(win_length):
+        w[lpad + n] = 0.5 - 0.5 * math.cos(2.0 * math.pi * n / win_length)
+    if normalized in (True, "window"):
+        scale = 1.0 / math.sqrt(sum(v * v for v in w))
+    elif normalized == "frame_length":
+        scale = 1.0 / math.sqrt(n_fft)
+    else:
+        scale = 1.0
+    frames = 1 + T // hop if center else 1 + (T - n_fft) // hop
+    out = np.zeros((n_fft // 2 + 1, frames))
+    for t in range(frames):
+        for k in range(n_fft // 2 + 1):
+            acc = 0j
+            for n in range(n_fft):
+                acc += sample(t * hop + n) * w[n] * scale * cmath.exp(-2j * math.pi * k * n / n_fft)
+            out[k, t] = abs(acc) ** power
+    return out
+
+
+def check_framing_brute_force(o):
+    """Every pad mode, with and without centring, the `pad` zeros and both
+    normalisations, against the sample-by-sample brute force."""
+    rng = np.random.default_rng(321)
+    cases = [  # n_fft, hop, win, T, pad
+        (8, 2, 8, 9, 0),
+        (8, 3, 6, 13, 2),
+        (10, 4, 10, 12, 0),
+        (12, 5, 12, 17, 3),
+    ]
+    for n_fft, hop, win, T, zp in cases:
+        x = rng.integers(-9, 10, size=T).astype(np.float32)
+        for mode in ("reflect", "constant", "replicate", "circular"):
+            for center in (True, False):
+                for norm in (False, "window", "frame_length"):
+                    ref = brute_power_framed(x, n_fft, hop, win, 2.0, center, mode, zp, norm)
+                    got = o.power_spectrogram(x, n_fft, hop, win, 2.0, center, mode, zp, norm)
+                    assert got.shape == ref.shape, (mode, center, got.shape, ref.shape)
+                    assert np.allclose(got, ref, rtol=1e-10, atol=1e-9 * max(1.0, ref.max())), (
+                        n_fft, hop, win, T, zp, mode, center, norm)
 
 
 # ------------------------------------------------------------ closed forms
@@ -199,8 +262,11 @@ def check_input_conversion(o):
 
 
 def check_torch_stft(o):
-    """Library special case: torch.stft, float64, centre reflect, periodic Hann."""
+    """Library special case: torch.stft, float64, periodic Hann, centre reflect
+    and every other framing torch offers (pad modes, no centring, `pad` zeros
+    first as torchaudio applies them, frame-length normalisation)."""
     import torch
+    import torch.nn.functional as tf
 
     rng = np.random.default_rng(11)
     for n_fft, hop, win, T in [(400, 160, 400, 3000), (1024, 256, 1024, 5000), (256, 64, 200, 1001)]:
@@ -213,6 +279,37 @@ def check_torch_stft(o):
         got = o.power_spectrogram(x, n_fft, hop, win, 2.0)
         assert got.shape == ref.shape
         assert np.allclose(got, ref, rtol=1e-9, atol=1e-9 * ref.max())
+    for n_fft, hop, win, T, zp in [(400, 160, 400, 1900, 0), (256, 64, 200, 1001, 37), (64, 16, 64, 300, 5)]:
+        x = rng.standard_normal(T)
+        w = torch.hann_window(win, periodic=True, dtype=torch.float64)
+        xt = tf.pad(torch.from_numpy(x)[None], (zp, zp), "constant")[0] if zp else torch.from_numpy(x)
+        for mode in ("reflect", "constant", "replicate", "circular"):
+            for center in (True, False):
+                for normalized in (False, True):
+                    S = torch.stft(xt, n_fft, hop, win, window=w, center=center, pad_mode=mode,
+                                   normalized=normalized, return_complex=True)
+                    ref = (S.abs() ** 2).numpy()
+                    got = o.power_spectrogram(x, n_fft, hop, win, 2.0, center, mode, zp,
+                                              "frame_length" if normalized else False)
+                    assert got.shape == ref.shape, (mode, center, got.shape, ref.shape)
+                    assert np.allclose(got, ref, rtol=1e-9, atol=1e-9 * ref.max()), (n_fft, mode, center, normalized)
+
+
+def check_window_normalisation(o):
+    """An impulse inside a frame gives |X[k]| = w[j] / sqrt(sum w^2) for every
+    k with the window normalisation (the frame-length one: w[j] / sqrt(N))."""
+    n_fft, hop, T, n0, win = 64, 16, 400, 211, 50
+    x = np.zeros(T)
+    x[n0] = 1.0
+    lpad = (n_fft - win) // 2
+    w = np.zeros(n_fft)
+    w[lpad : lpad + win] = [0.5 - 0.5 * math.cos(2.0 * math.pi * n / win) for n in range(win)]
+    for normalized, scale in (("window", 1.0 / math.sqrt(float(np.dot(w, w)))), ("frame_length", 1.0 / 8.0)):
+        P = o.power_spectrogram(x, n_fft, hop, win, 1.0, True, "reflect", 0, normalized)
+        for t in range(P.shape[1]):
+            j = n0 + n_fft // 2 - t * hop
+            expect = w[j] * scale if 0 <= j < n_fft else 0.0
+            assert np.allclose(P[:, t], expect, rtol=1e-12, atol=1e-15), (normalized, t)
 
 
 ALL_CHECKS = [
@@ -225,4 +322,6 @@ ALL_CHECKS = [
     check_slaney_area,
     check_input_conversion,
     check_torch_stft,
+    check_framing_brute_force,
+    check_window_normalisation,
 ]

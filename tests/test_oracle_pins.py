@@ -129,6 +129,64 @@ def _power_half(o):
     o.spectral_power = sp
 
 
+def _circular_shifted(o):
+    orig = o.centre_pad
+
+    def cp(x, pad, mode):
+        if mode == "circular":
+            T = x.shape[-1]
+            return x[..., (np.arange(-pad, T + pad) + 1) % T]  # wraps one sample late
+        return orig(x, pad, mode)
+
+    o.centre_pad = cp
+
+
+def _replicate_inner_sample(o):
+    orig = o.centre_pad
+
+    def cp(x, pad, mode):
+        if mode == "replicate":
+            T = x.shape[-1]
+            return x[..., np.clip(np.arange(-pad, T + pad), 1, T - 2)]  # repeats the second sample
+        return orig(x, pad, mode)
+
+    o.centre_pad = cp
+
+
+def _zero_pad_after_centring(o):
+    def ps(x, n_fft, hop, win_length=None, power=2.0, center=True, pad_mode="reflect", pad=0, normalized=False):
+        win_length = n_fft if win_length is None else win_length
+        xd = o.to_float64(x)
+        T = xd.shape[-1] + 2 * pad
+        if center:
+            xp = o.zero_pad(o.centre_pad(xd, n_fft // 2, pad_mode), pad)  # zeros outside the centre pad
+            count = o.n_frames(T, hop)
+        else:
+            xp = o.zero_pad(xd, pad)
+            count = o.n_frames_uncentred(T, n_fft, hop)
+        frames = o.frame(xp, n_fft, hop, count)
+        w = o.hann_periodic(win_length, n_fft)
+        return np.swapaxes(o.spectral_power(o.dft_onesided(frames * w * o.window_norm(w, n_fft, normalized)), power),
+                           -1, -2)
+
+    o.power_spectrogram = ps
+
+
+def _window_norm_linear_sum(o):
+    orig = o.window_norm
+
+    def wn(w, n_fft, normalized):
+        if normalized in (True, "window"):
+            return 1.0 / float(np.sum(w))
+        return orig(w, n_fft, normalized)
+
+    o.window_norm = wn
+
+
+def _uncentred_frame_count(o):
+    o.n_frames_uncentred = lambda T, n_fft, hop: 1 + (T - n_fft + hop - 1) // hop
+
+
 MUTANTS = [
     _symmetric_hann,
     _edge_repeating_pad,
@@ -139,6 +197,11 @@ MUTANTS = [
     _htk_natural_log,
     _int16_scale,
     _power_half,
+    _circular_shifted,
+    _replicate_inner_sample,
+    _zero_pad_after_centring,
+    _window_norm_linear_sum,
+    _uncentred_frame_count,
 ]
 
 
