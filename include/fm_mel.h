@@ -8,9 +8,11 @@
  *   out[b, m, t] = sum_k F[m, k] * |X_{b,t}[k]|^power
  *   X_{b,t}[k]   = sum_{n < n_fft} xp_b[t*hop + n] * w[n] * exp(-2 pi i k n / n_fft)
  *
- * with xp_b the signal reflect-padded by n_fft/2 on both sides (centre=True,
- * pad_mode="reflect"), w the periodic Hann window of win_length samples
- * zero-padded and centred to n_fft, k = 0 .. n_fft/2, t = 0 .. T/hop, and F
+ * with xp_b the signal padded for framing (by default reflect-padded by
+ * n_fft/2 on both sides, torchaudio's center=True, pad_mode="reflect";
+ * fm_plan_create_ex selects the other torchaudio framings), w the periodic
+ * Hann window of win_length samples zero-padded and centred to n_fft (scaled
+ * by the chosen STFT normalisation), k = 0 .. n_fft/2, t over the frames, and F
  * the triangular mel filterbank (HTK or Slaney mel scale, optional Slaney
  * area norm) over bins at frequency k*sr/n_fft.
  *
@@ -50,6 +52,13 @@ typedef enum {
 typedef enum { FM_MEL_HTK = 0, FM_MEL_SLANEY = 1 } fm_mel_scale;
 typedef enum { FM_NORM_NONE = 0, FM_NORM_SLANEY = 1 } fm_norm;
 typedef enum { FM_F32 = 0, FM_I16 = 1, FM_F16 = 2 } fm_dtype;
+/* torch's pad modes for the centre padding: mirror without repeating the
+ * edge sample, zeros, repeat the edge sample, wrap around the signal */
+typedef enum { FM_PAD_REFLECT = 0, FM_PAD_CONSTANT = 1, FM_PAD_REPLICATE = 2, FM_PAD_CIRCULAR = 3 } fm_pad_mode;
+/* STFT normalisation, folded into the window: none, divide by
+ * sqrt(sum w^2) (torchaudio normalized=True / "window"), or by sqrt(n_fft)
+ * ("frame_length", torch.stft normalized=True) */
+typedef enum { FM_NORMALIZED_NONE = 0, FM_NORMALIZED_WINDOW = 1, FM_NORMALIZED_FRAME_LENGTH = 2 } fm_normalized;
 
 /*
  * fm_plan_create -- validate the transform parameters and build its tables.
@@ -91,14 +100,53 @@ fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, int win_leng
                          double f_min, double f_max, double power, fm_mel_scale mel_scale,
                          fm_norm norm, fm_dtype in_dtype, fm_dtype out_dtype);
 
+/*
+ * fm_plan_create_ex -- fm_plan_create with the framing options too.
+ *
+ * flashmel README "Usage": every torchaudio.transforms.MelSpectrogram
+ * argument except window_fn / wkwargs, including pad, center, pad_mode and
+ * normalized; "How it works": the padding (pad, center, all four pad modes)
+ * is applied as index arithmetic and the normalized modes are folded into
+ * the window on the host.
+ *
+ * The first twelve fields mean what fm_plan_create's arguments of the same
+ * names mean. Then:
+ *   center     : nonzero pads n_fft/2 samples on both sides by pad_mode
+ *                before framing (frames = 1 + floor(T' / hop)); zero frames
+ *                the signal as it is (frames = 1 + floor((T' - n_fft) / hop)),
+ *                with T' = T + 2 * pad.
+ *   pad_mode   : fm_pad_mode of the centre padding (ignored without center).
+ *   pad        : zeros added on both sides of every signal before the centre
+ *                padding (torchaudio's `pad`), 0 .. 2^20.
+ *   normalized : fm_normalized.
+ * fm_plan_create(...) is fm_plan_create_ex with center = 1, FM_PAD_REFLECT,
+ * pad = 0 and FM_NORMALIZED_NONE. `params` is read during the call only.
+ * Errors: as fm_plan_create, plus FM_ERR_INVALID_ARG for NULL params or an
+ * option out of range.
+ */
+typedef struct {
+  int sr, n_fft, hop, win_length, n_mels;
+  double f_min, f_max, power;
+  fm_mel_scale mel_scale;
+  fm_norm norm;
+  fm_dtype in_dtype, out_dtype;
+  int center;
+  fm_pad_mode pad_mode;
+  int pad;
+  fm_normalized normalized;
+} fm_plan_params;
+
+fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* params);
+
 /* fm_plan_destroy -- free the plan's device tables. NULL is accepted (no-op).
  * Work already queued with the plan must have finished (e.g. synchronise the
  * streams first). Returns FM_OK, or FM_ERR_CUDA if freeing failed. */
 fm_status fm_plan_destroy(fm_plan* plan);
 
-/* fm_n_frames -- frames per signal for T samples with centre padding:
- * 1 + floor(T / hop) (torch.stft, center=True). Returns -1 if plan is NULL or
- * T < 0. */
+/* fm_n_frames -- frames per signal for T samples: with T' = T + 2 * pad,
+ * 1 + floor(T' / hop) when centred, 1 + floor((T' - n_fft) / hop) when not
+ * (torch.stft). Returns -1 if plan is NULL or T is too short for the plan's
+ * framing (see fm_mel_forward). */
 int64_t fm_n_frames(const fm_plan* plan, int64_t T);
 
 /*
@@ -110,8 +158,10 @@ int64_t fm_n_frames(const fm_plan* plan, int64_t T);
  *            contiguous, any alignment of the element type. Not modified.
  *   B      : number of signals, >= 0. B == 0 returns FM_OK and does nothing
  *            (d_in / d_out may then be NULL).
- *   T      : samples per signal; must exceed n_fft/2 (a reflect pad cannot be
- *            longer than the signal).
+ *   T      : samples per signal, >= 1. With T' = T + 2 * pad: centred
+ *            reflect padding needs T' > n_fft/2 and circular T' >= n_fft/2
+ *            (a mirror or a wrap cannot reach further); without centring
+ *            T' >= n_fft (one whole frame).
  *   d_out  : device pointer, [B][n_mels][fm_n_frames(T)] of the plan's
  *            out_dtype, contiguous, element-aligned; fully overwritten. Must
  *            not overlap d_in.
@@ -120,7 +170,8 @@ int64_t fm_n_frames(const fm_plan* plan, int64_t T);
  * Allocates nothing and does not synchronise. Both buffers are owned by the
  * caller and must stay valid until the stream reaches this work.
  * Errors: FM_ERR_INVALID_ARG (NULL plan or pointer with B > 0, B < 0,
- * T <= n_fft/2, B*T or the output size beyond 2^62 elements); FM_ERR_CUDA
+ * T too short for the framing, B*T or the output size beyond 2^62
+ * elements); FM_ERR_CUDA
  * (launch failed, or called on another device than the plan's).
  */
 fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64_t B, int64_t T, void* d_out,
@@ -207,6 +258,7 @@ typedef struct {
   int grid_limit;         /* persistent grid size = SMs x blocks_per_sm */
   int smem_bytes;         /* dynamic shared memory per CTA */
   int device;             /* CUDA device the plan lives on */
+  int center, pad_mode, pad, normalized;  /* the framing options (fm_plan_create_ex) */
 } fm_plan_info;
 
 /* fm_plan_get_info -- fill *info. FM_ERR_INVALID_ARG on NULL arguments. */

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     fm_mel_forward_host_noalloc,
     fm_n_frames,
     fm_plan_create,
+    fm_plan_create_ex,
     fm_plan_destroy,
     fm_plan_get_info,
     fm_plan_poll_error,

@@ -16,10 +16,13 @@ FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_CUDA, FM_ERR_OOM, FM_ERR_K
 FM_MEL_HTK, FM_MEL_SLANEY = 0, 1
 FM_NORM_NONE, FM_NORM_SLANEY = 0, 1
 FM_F32, FM_I16, FM_F16 = 0, 1, 2
+FM_PAD_REFLECT, FM_PAD_CONSTANT, FM_PAD_REPLICATE, FM_PAD_CIRCULAR = 0, 1, 2, 3
+FM_NORMALIZED_NONE, FM_NORMALIZED_WINDOW, FM_NORMALIZED_FRAME_LENGTH = 0, 1, 2
 
 # every symbol include/fm_mel.h declares
 EXPORTS = [
     "fm_plan_create",
+    "fm_plan_create_ex",
     "fm_plan_destroy",
     "fm_n_frames",
     "fm_mel_forward",
@@ -44,6 +47,16 @@ class fm_plan_info(C.Structure):
         ("in_dtype", C.c_int), ("out_dtype", C.c_int), ("nnz", C.c_int64), ("frames_per_tile", C.c_int),
         ("threads_per_block", C.c_int), ("blocks_per_sm", C.c_int), ("grid_limit", C.c_int),
         ("smem_bytes", C.c_int), ("device", C.c_int),
+        ("center", C.c_int), ("pad_mode", C.c_int), ("pad", C.c_int), ("normalized", C.c_int),
+    ]
+
+
+class fm_plan_params(C.Structure):
+    _fields_ = [
+        ("sr", C.c_int), ("n_fft", C.c_int), ("hop", C.c_int), ("win_length", C.c_int), ("n_mels", C.c_int),
+        ("f_min", C.c_double), ("f_max", C.c_double), ("power", C.c_double),
+        ("mel_scale", C.c_int), ("norm", C.c_int), ("in_dtype", C.c_int), ("out_dtype", C.c_int),
+        ("center", C.c_int), ("pad_mode", C.c_int), ("pad", C.c_int), ("normalized", C.c_int),
     ]
 
 
@@ -64,6 +77,8 @@ def lib() -> C.CDLL:
     vp, i64, ci, cd = C.c_void_p, C.c_int64, C.c_int, C.c_double
     L.fm_plan_create.argtypes = [C.POINTER(vp), ci, ci, ci, ci, ci, cd, cd, cd, ci, ci, ci, ci]
     L.fm_plan_create.restype = ci
+    L.fm_plan_create_ex.argtypes = [C.POINTER(vp), C.POINTER(fm_plan_params)]
+    L.fm_plan_create_ex.restype = ci
     L.fm_plan_destroy.argtypes = [vp]
     L.fm_plan_destroy.restype = ci
     L.fm_n_frames.argtypes = [vp, i64]
@@ -98,6 +113,11 @@ def _check(status: int, what: str) -> None:
 _SCALES = {"htk": FM_MEL_HTK, "slaney": FM_MEL_SLANEY}
 _NORMS = {None: FM_NORM_NONE, "none": FM_NORM_NONE, "slaney": FM_NORM_SLANEY}
 _DTYPES = {"f32": FM_F32, "i16": FM_I16, "f16": FM_F16}
+_PAD_MODES = {"reflect": FM_PAD_REFLECT, "constant": FM_PAD_CONSTANT, "replicate": FM_PAD_REPLICATE,
+              "circular": FM_PAD_CIRCULAR}
+_NORMALIZED = {False: FM_NORMALIZED_NONE, None: FM_NORMALIZED_NONE, "none": FM_NORMALIZED_NONE,
+               True: FM_NORMALIZED_WINDOW, "window": FM_NORMALIZED_WINDOW,
+               "frame_length": FM_NORMALIZED_FRAME_LENGTH}
 
 
 def fm_plan_create(sr, n_fft, hop, win_length, n_mels, f_min, f_max, power, mel_scale="htk", norm=None,
@@ -110,6 +130,23 @@ def fm_plan_create(sr, n_fft, hop, win_length, n_mels, f_min, f_max, power, mel_
         _NORMS.get(norm, norm), _DTYPES.get(in_dtype, in_dtype), _DTYPES.get(out_dtype, out_dtype),
     )
     _check(st, "fm_plan_create")
+    return h.value
+
+
+def fm_plan_create_ex(sr, n_fft, hop, win_length, n_mels, f_min, f_max, power, mel_scale="htk", norm=None,
+                      in_dtype="f32", out_dtype="f32", center=True, pad_mode="reflect", pad=0,
+                      normalized=False) -> int:
+    """fm_plan_create with torchaudio's framing options (center, pad_mode,
+    pad, normalized as False / True / "window" / "frame_length")."""
+    p = fm_plan_params(
+        int(sr), int(n_fft), int(hop), int(win_length or 0), int(n_mels), float(f_min),
+        float(f_max if f_max is not None else 0.0), float(power), _SCALES.get(mel_scale, mel_scale),
+        _NORMS.get(norm, norm), _DTYPES.get(in_dtype, in_dtype), _DTYPES.get(out_dtype, out_dtype),
+        1 if center else 0, _PAD_MODES.get(pad_mode, pad_mode), int(pad),
+        _NORMALIZED[normalized] if isinstance(normalized, (bool, str, type(None))) else int(normalized),
+    )
+    h = C.c_void_p()
+    _check(lib().fm_plan_create_ex(C.byref(h), C.byref(p)), "fm_plan_create_ex")
     return h.value
 
 

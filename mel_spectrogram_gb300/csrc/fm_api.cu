@@ -32,6 +32,7 @@ const Variant* find_variant(int n_fft, int hop) {
 struct fm_plan {
   int device;
   int sr, n_fft, hop, win_length, n_mels;
+  int center, pad_mode, zpad, normalized;  // framing options (fm_plan_create_ex)
   double f_min, f_max, power;
   int mel_scale, norm, in_dtype, out_dtype, power_mode;
   const fm::Variant* var;
@@ -157,8 +158,8 @@ void encode_input_map(const fm_plan* plan, const void* d_in, int64_t B, int64_t 
   const int64_t line = (int64_t)kh * plan->hop;
   const int64_t pitch = (int64_t)fm::in_row_stride_x2((int)line, (int)esize) * esize;  // bytes per staged row
   const int64_t rows = fm::x2_lines(plan->n_fft, plan->hop, kh);
-  const int64_t pad = plan->n_fft / 2;
-  const int64_t off = ((-pad) % line + line) % line;
+  const int64_t lead = (plan->center ? plan->n_fft / 2 : 0) + plan->zpad;  // padding before sample 0
+  const int64_t off = ((-lead) % line + line) % line;
   const uintptr_t base = reinterpret_cast<uintptr_t>(d_in) + (uintptr_t)(off * esize);
   if ((line * esize) % 16 != 0 || (T * esize) % 16 != 0 || base % 16 != 0) return;
   if (pitch / 8 > 256 || rows > 256 || B > ((int64_t)1 << 31) || T - off < line) return;
@@ -188,8 +189,42 @@ fm_status from_cuda(cudaError_t e) {
 extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, int win_length, int n_mels,
                                     double f_min, double f_max, double power, fm_mel_scale mel_scale,
                                     fm_norm norm, fm_dtype in_dtype, fm_dtype out_dtype) {
+  fm_plan_params p;
+  p.sr = sr;
+  p.n_fft = n_fft;
+  p.hop = hop;
+  p.win_length = win_length;
+  p.n_mels = n_mels;
+  p.f_min = f_min;
+  p.f_max = f_max;
+  p.power = power;
+  p.mel_scale = mel_scale;
+  p.norm = norm;
+  p.in_dtype = in_dtype;
+  p.out_dtype = out_dtype;
+  p.center = 1;
+  p.pad_mode = FM_PAD_REFLECT;
+  p.pad = 0;
+  p.normalized = FM_NORMALIZED_NONE;
+  return fm_plan_create_ex(out, &p);
+}
+
+extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* params) {
   if (out == nullptr) return FM_ERR_INVALID_ARG;
   *out = nullptr;
+  if (params == nullptr) return FM_ERR_INVALID_ARG;
+  const int sr = params->sr, n_fft = params->n_fft, hop = params->hop, n_mels = params->n_mels;
+  int win_length = params->win_length;
+  const double f_min = params->f_min, power = params->power;
+  double f_max = params->f_max;
+  const fm_mel_scale mel_scale = params->mel_scale;
+  const fm_norm norm = params->norm;
+  const fm_dtype in_dtype = params->in_dtype, out_dtype = params->out_dtype;
+  const int center = params->center ? 1 : 0, pad_mode = (int)params->pad_mode, zpad = params->pad;
+  const int normalized = (int)params->normalized;
+  if (pad_mode < FM_PAD_REFLECT || pad_mode > FM_PAD_CIRCULAR) return FM_ERR_INVALID_ARG;
+  if (zpad < 0 || zpad > (1 << 20)) return FM_ERR_INVALID_ARG;
+  if (normalized < FM_NORMALIZED_NONE || normalized > FM_NORMALIZED_FRAME_LENGTH) return FM_ERR_INVALID_ARG;
   if (win_length == 0) win_length = n_fft;
   if (sr <= 0 || n_fft <= 0 || hop <= 0 || n_mels <= 0) return FM_ERR_INVALID_ARG;
   if (win_length < 0 || win_length > n_fft) return FM_ERR_INVALID_ARG;
@@ -209,7 +244,8 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   try {
     fm::build_filterbank(sr, n_fft, n_mels, f_min, f_max, mel_scale == FM_MEL_SLANEY, norm == FM_NORM_SLANEY, ms,
                          ml, mo, mw);
-    fm::build_window(n_fft, win_length, win);
+    // the STFT normalisation is folded into the window (README "How it works")
+    fm::build_window(n_fft, win_length, normalized, win);
     fm::build_twiddles(n_fft / 2, n_fft / 2, twh);
     fm::build_twiddles(n_fft, n_fft / 2 + 1, twf);
   } catch (const std::bad_alloc&) {
@@ -247,6 +283,10 @@ extern "C" fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, i
   if (p == nullptr) return FM_ERR_OOM;
   p->x2 = nullptr;
   p->device = dev;
+  p->center = center;
+  p->pad_mode = pad_mode;
+  p->zpad = zpad;
+  p->normalized = normalized;
   p->sr = sr;
   p->n_fft = n_fft;
   p->hop = hop;
@@ -361,20 +401,29 @@ extern "C" fm_status fm_plan_destroy(fm_plan* plan) {
   return e == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
-extern "C" int64_t fm_n_frames(const fm_plan* plan, int64_t T) {
-  if (plan == nullptr || T < 0) return -1;
-  return 1 + T / plan->hop;
+// Frames for T samples under the plan's framing, or -1 if T is too short for
+// it: with T' = T + 2 pad, centred reflect needs T' > n_fft/2 (a mirror cannot
+// reach further), centred circular T' >= n_fft/2, centred constant and
+// replicate T >= 1, uncentred T' >= n_fft.
+static int64_t frames_for(const fm_plan* plan, int64_t T) {
+  if (plan == nullptr || T < 1 || T > ((int64_t)1 << 61)) return -1;
+  const int64_t Tp = T + 2 * (int64_t)plan->zpad, c = plan->n_fft / 2;
+  if (!plan->center) return Tp >= plan->n_fft ? 1 + (Tp - plan->n_fft) / plan->hop : -1;
+  if (plan->pad_mode == FM_PAD_REFLECT && Tp <= c) return -1;
+  if (plan->pad_mode == FM_PAD_CIRCULAR && Tp < c) return -1;
+  return 1 + Tp / plan->hop;
 }
+
+extern "C" int64_t fm_n_frames(const fm_plan* plan, int64_t T) { return frames_for(plan, T); }
 
 static fm_status check_forward(const fm_plan* plan, const void* in, int64_t B, int64_t T, const void* out) {
   if (plan == nullptr || B < 0) return FM_ERR_INVALID_ARG;
   if (B == 0) return FM_OK;
   if (in == nullptr || out == nullptr) return FM_ERR_INVALID_ARG;
-  if (T <= plan->n_fft / 2) return FM_ERR_INVALID_ARG;
+  const int64_t nf = frames_for(plan, T);
+  if (nf < 1 || nf > INT_MAX) return FM_ERR_INVALID_ARG;
   const int64_t lim = (int64_t)1 << 62;
   if (T > lim / B) return FM_ERR_INVALID_ARG;
-  const int64_t nf = 1 + T / plan->hop;
-  if (nf > INT_MAX) return FM_ERR_INVALID_ARG;
   if (nf * plan->n_mels > lim / B) return FM_ERR_INVALID_ARG;
   return FM_OK;
 }
@@ -392,9 +441,12 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.out = d_out;
   prm.B = B;
   prm.T = T;
-  prm.n_frames = (int)(1 + T / plan->hop);
+  prm.n_frames = (int)frames_for(plan, T);
   prm.hop = plan->hop;
-  prm.pad = plan->n_fft / 2;
+  prm.cpad = plan->center ? plan->n_fft / 2 : 0;
+  prm.zpad = plan->zpad;
+  prm.lead = prm.cpad + prm.zpad;
+  prm.pad_mode = plan->pad_mode;
   prm.in_dtype = plan->in_dtype;
   prm.out_dtype = plan->out_dtype;
   prm.n_mels = plan->n_mels;
@@ -443,7 +495,7 @@ extern "C" fm_status fm_mel_forward_host(const fm_plan* plan, const void* h_in, 
   if (d_in_scratch == nullptr || d_out_scratch == nullptr) return FM_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t in_bytes = (size_t)B * (size_t)T * dtype_size(plan->in_dtype);
-  const size_t out_bytes = (size_t)B * plan->n_mels * (size_t)(1 + T / plan->hop) * dtype_size(plan->out_dtype);
+  const size_t out_bytes = (size_t)B * plan->n_mels * (size_t)frames_for(plan, T) * dtype_size(plan->out_dtype);
   if (cudaMemcpyAsync(d_in_scratch, h_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return FM_ERR_CUDA;
   st = fm_mel_forward(plan, d_in_scratch, B, T, d_out_scratch, stream);
   if (st != FM_OK) return st;
@@ -468,6 +520,10 @@ extern "C" fm_status fm_plan_get_info(const fm_plan* plan, fm_plan_info* info) {
   info->grid_limit = plan->grid_limit;
   info->smem_bytes = (int)plan->smem;
   info->device = plan->device;
+  info->center = plan->center;
+  info->pad_mode = plan->pad_mode;
+  info->pad = plan->zpad;
+  info->normalized = plan->normalized;
   return FM_OK;
 }
 

@@ -95,15 +95,22 @@ void build_filterbank(int sr, int n_fft, int n_mels, double f_min, double f_max,
   off[n_mels] = (int)weights.size();
 }
 
-void build_window(int n_fft, int win_length, std::vector<float>& window) {
+void build_window(int n_fft, int win_length, int normalized, std::vector<float>& window) {
   // periodic Hann of win_length samples, zero-padded and centred in n_fft;
+  // times the STFT normalisation (1, 1/sqrt(sum w^2) or 1/sqrt(n_fft)) and
   // times 1/2, the factor of the real-FFT split that the kernel leaves out.
   window.assign(n_fft, 0.0f);
   const int left = (n_fft - win_length) / 2;
+  std::vector<double> w(win_length);
+  double energy = 0.0;
   for (int n = 0; n < win_length; ++n) {
-    const double w = 0.5 - 0.5 * std::cos(kTwoPi * (double)n / (double)win_length);
-    window[left + n] = (float)(0.5 * w);
+    w[n] = 0.5 - 0.5 * std::cos(kTwoPi * (double)n / (double)win_length);
+    energy += w[n] * w[n];
   }
+  double scale = 1.0;
+  if (normalized == FM_NORMALIZED_WINDOW) scale = 1.0 / std::sqrt(energy);
+  else if (normalized == FM_NORMALIZED_FRAME_LENGTH) scale = 1.0 / std::sqrt((double)n_fft);
+  for (int n = 0; n < win_length; ++n) window[left + n] = (float)(0.5 * scale * w[n]);
 }
 
 void build_twiddles(int len, int count, std::vector<float2>& tw) {

@@ -20,8 +20,9 @@ void build_filterbank(int sr, int n_fft, int n_mels, double f_min, double f_max,
                       bool slaney_norm, std::vector<int>& start, std::vector<int>& len,
                       std::vector<int>& off, std::vector<float>& weights);
 
-// Periodic Hann (times 1/2), zero-padded and centred to n_fft.
-void build_window(int n_fft, int win_length, std::vector<float>& window);
+// Periodic Hann (times 1/2 and the fm_normalized scale), zero-padded and
+// centred to n_fft.
+void build_window(int n_fft, int win_length, int normalized, std::vector<float>& window);
 
 // tw[j] = exp(-2 pi i j / len), j < count, stored (cos, -sin).
 void build_twiddles(int len, int count, std::vector<float2>& tw);

@@ -17,7 +17,11 @@ struct KernelParams {
   long long B, T;
   int n_frames;
   int hop;
-  int pad;  // n_fft / 2
+  // framing: frame t covers samples [t * hop - lead, t * hop - lead + n_fft)
+  // of the signal; outside [0, T) the `zpad` zeros of torchaudio's `pad`, then
+  // `cpad` centre-padding samples by pad_mode (FM_PAD_*), then nothing that a
+  // valid frame reads
+  int lead, zpad, cpad, pad_mode;
   int in_dtype, out_dtype;
   int n_mels;
   int nnz;

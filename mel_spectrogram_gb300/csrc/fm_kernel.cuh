@@ -149,17 +149,42 @@ __device__ __forceinline__ Raw raw_zero() {
   else return Raw(0);
 }
 
+// Framing of one signal outside its samples [0, T): zpad zeros on each side
+// (torchaudio's `pad`), then cpad samples of centre padding by mode.
+struct PadSpec {
+  int zpad, cpad, mode;
+};
+
+// The signal index whose sample stands at position s (< 0 or >= T) of the
+// padded signal, or -1 for a zero: one of the `pad` zeros, constant centre
+// padding, or a position past the padded signal (no valid frame reads it).
+// With T' = T + 2 zpad and j = s + zpad the index in the zero-padded signal:
+// reflect mirrors j about its first / last sample without repeating it,
+// replicate repeats the edge, circular wraps by T' (torch's pad modes).
+__device__ __forceinline__ long long padded_source(long long s, long long T, const PadSpec& ps) {
+  if (s >= 0 && s < T) return s;
+  const long long Tp = T + 2 * (long long)ps.zpad;
+  long long j = s + ps.zpad;
+  if (j >= 0 && j < Tp) return -1;
+  if (j < -(long long)ps.cpad || j >= Tp + ps.cpad) return -1;
+  if (ps.mode == FM_PAD_REFLECT) j = j < 0 ? -j : 2 * (Tp - 1) - j;
+  else if (ps.mode == FM_PAD_REPLICATE) j = j < 0 ? 0 : Tp - 1;
+  else if (ps.mode == FM_PAD_CIRCULAR) j = j < 0 ? j + Tp : j - Tp;
+  else return -1;
+  const long long src = j - ps.zpad;
+  return (src >= 0 && src < T) ? src : -1;
+}
+
 // Stage rows [0, rows) of hop samples starting at signal index gstart of
 // signal row `src` (length T) into dst (row stride S elements), as
 // asynchronous copies wherever possible: aligned in-range sample pairs as one
-// 8- or 4-byte cp.async; otherwise element by element, mirrored about the
-// first/last sample (reflect padding), f32 still by 4-byte cp.async and
-// 16-bit samples by plain loads (only the few mirrored or misaligned ones).
-// Positions past the padded signal are zero (no valid frame reads them).
+// 8- or 4-byte cp.async; otherwise element by element through
+// padded_source (the padding of `ps`), f32 still by 4-byte cp.async and
+// 16-bit samples by plain loads (only the few padded or misaligned ones).
 // The caller commits the group, waits for it and then synchronises the CTA.
 template <typename Raw, int NWARPS>
 __device__ __forceinline__ void stage_tile(const Raw* __restrict__ src, long long T, long long gstart, int rows,
-                                           int hop, int S, Raw* dst, int warp, int lane) {
+                                           int hop, int S, Raw* dst, int warp, int lane, const PadSpec& ps) {
   const bool interior = gstart >= 0 && gstart + (long long)rows * hop <= T;
   const bool aligned = ((reinterpret_cast<uintptr_t>(src + gstart)) % (2 * sizeof(Raw))) == 0;
   const int pairs = hop / 2;
@@ -182,11 +207,9 @@ __device__ __forceinline__ void stage_tile(const Raw* __restrict__ src, long lon
       }
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        long long se = s + e;
-        if (se < 0) se = -se;                   // mirror about the first sample
-        else if (se >= T) se = 2 * T - 2 - se;  // mirror about the last sample
+        const long long se = padded_source(s + e, T, ps);
         Raw* de = d + 2 * c2 + e;
-        if (se < 0 || se >= T) {
+        if (se < 0) {
           *de = raw_zero<Raw>();
         } else if constexpr (sizeof(Raw) == 4) {
           cp_async<4>(de, src + se);
@@ -417,13 +440,14 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
   const Raw* in = static_cast<const Raw*>(prm.in);
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
+  const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
   auto in_buf = [&](int i) { return reinterpret_cast<Raw*>(smem + lay.in_tile + (size_t)i * lay.in_tile_bytes); };
   auto stage = [&](long long tile, int buf) {
     long long b;
     int tt;
     split(tile, b, tt);
     const long long t0 = (long long)tt * G;
-    stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.pad, rows, hop, S, in_buf(buf), warp, lane);
+    stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.lead, rows, hop, S, in_buf(buf), warp, lane, pads);
     cp_async_commit();
   };
 

@@ -272,20 +272,22 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
   const Raw* in = static_cast<const Raw*>(prm.in);
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
+  const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
   unsigned long long* full = reinterpret_cast<unsigned long long*>(smem + lay.bars);
   unsigned long long* empty = full + kX2Groups;
   auto stage = [&](int g, long long tile) {
     long long b;
     int tt;
     split(tile, b, tt);
-    const long long gstart = (long long)tt * kX2Frames * st.hop - prm.pad;
+    const long long gstart = (long long)tt * kX2Frames * st.hop - prm.lead;
     const Raw* sig = in + b * T;
     Raw* dst = reinterpret_cast<Raw*>(smem + lay.in_tile + g * lay.group_stride);
     const long long L = st.line;
-    // lines [r_lo, r_hi) lie inside [0, T); lines from r_end on start past T + pad
+    // lines [r_lo, r_hi) lie inside [0, T); lines from r_end on start past
+    // the padded signal (T + zpad + cpad)
     long long r_lo = gstart >= 0 ? 0 : (-gstart + L - 1) / L;
     long long r_hi = (T - gstart) / L;
-    long long r_end = (T + prm.pad - gstart + L - 1) / L;
+    long long r_end = (T + prm.zpad + prm.cpad - gstart + L - 1) / L;
     r_end = r_end < st.rows ? r_end : st.rows;
     r_hi = r_hi < r_end ? r_hi : r_end;
     const bool tma_ok = ((st.line * esize) & 15) == 0 && (reinterpret_cast<uintptr_t>(sig + gstart) & 15) == 0;
@@ -309,11 +311,11 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     __syncwarp();
     for (int r = (int)r_lo + lane; r < (int)r_hi; r += 32)
       tma_load_1d(dst + r * st.S, sig + gstart + r * L, (unsigned)(L * esize), full + g);
-    if (r_lo > 0) stage_tile<Raw, 1>(sig, T, gstart, (int)r_lo, st.line, st.S, dst, 0, lane);
+    if (r_lo > 0) stage_tile<Raw, 1>(sig, T, gstart, (int)r_lo, st.line, st.S, dst, 0, lane, pads);
     const int r_tail = (int)(r_hi > r_lo ? r_hi : r_lo);
     if (r_end > r_tail)
       stage_tile<Raw, 1>(sig, T, gstart + r_tail * L, (int)r_end - r_tail, st.line, st.S, dst + r_tail * st.S, 0,
-                         lane);
+                         lane, pads);
     cp_async_commit();
     cp_async_wait_all();
     __syncwarp();  // every lane's element copies have landed

@@ -56,11 +56,11 @@ extern "C" fm_status fm_mel_forward_host_noalloc(const fm_plan* plan, const void
   fm_plan_info info;
   fm_status st = fm_plan_get_info(plan, &info);
   if (st != FM_OK) return st;
-  if (T <= info.n_fft / 2) return FM_ERR_INVALID_ARG;
+  const int64_t n_frames = fm_n_frames(plan, T);  // -1 if T is too short for the plan's framing
+  if (n_frames < 1) return FM_ERR_INVALID_ARG;
   // sizes, checked against the array before any product can overflow
   const int64_t cap = (int64_t)kStagingBytes;
   if (B > cap || T > cap / B) return FM_ERR_INVALID_ARG;
-  const int64_t n_frames = 1 + T / info.hop;
   if (n_frames > cap / B || (int64_t)info.n_mels > cap / (B * n_frames)) return FM_ERR_INVALID_ARG;
   const size_t in_bytes = (size_t)B * (size_t)T * dtype_bytes(info.in_dtype);
   const size_t out_bytes = (size_t)B * (size_t)info.n_mels * (size_t)n_frames * dtype_bytes(info.out_dtype);

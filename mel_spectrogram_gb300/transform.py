@@ -2,8 +2,9 @@
 
 flashmel README, "Usage": MelSpectrogram(torchaudio arguments, dtype=...)(x)
 with x of shape (..., time) on the GPU, float32 or int16 PCM (here also
-float16), returning (..., n_mels, n_frames) in float32 or float16. Centre
-reflect padding and the periodic Hann window are fixed, as in the configs.
+float16), returning (..., n_mels, n_frames) in float32 or float16, with the
+torchaudio arguments pad, center, pad_mode and normalized. The window is
+always the periodic Hann (no window_fn), the spectrum one-sided.
 """
 from __future__ import annotations
 
@@ -14,8 +15,16 @@ class MelSpectrogram:
     """Callable mel transform; owns one plan per (device, input dtype)."""
 
     def __init__(self, sample_rate=16000, n_fft=400, win_length=None, hop_length=None, f_min=0.0, f_max=None,
-                 n_mels=128, power=2.0, mel_scale="htk", norm=None, dtype=None):
+                 pad=0, n_mels=128, power=2.0, normalized=False, center=True, pad_mode="reflect", onesided=True,
+                 norm=None, mel_scale="htk", dtype=None):
         import torch
+
+        if not onesided:
+            raise ValueError("onesided=False is not supported (the mel scale takes one-sided spectra)")
+        self.pad = int(pad)
+        self.normalized = normalized
+        self.center = bool(center)
+        self.pad_mode = pad_mode
 
         self.sample_rate = int(sample_rate)
         self.n_fft = int(n_fft)
@@ -38,15 +47,19 @@ class MelSpectrogram:
         key = (device_index, in_dtype)
         if key not in self._plans:
             with torch.cuda.device(device_index):
-                self._plans[key] = fb.fm_plan_create(
+                self._plans[key] = fb.fm_plan_create_ex(
                     self.sample_rate, self.n_fft, self.hop_length, self.win_length, self.n_mels, self.f_min,
                     self.f_max, self.power, self.mel_scale, self.norm, in_dtype,
-                    "f16" if self.dtype == torch.float16 else "f32",
+                    "f16" if self.dtype == torch.float16 else "f32", self.center, self.pad_mode, self.pad,
+                    self.normalized,
                 )
         return self._plans[key]
 
     def n_frames(self, T: int) -> int:
-        return 1 + int(T) // self.hop_length
+        Tp = int(T) + 2 * self.pad
+        if self.center:
+            return 1 + Tp // self.hop_length
+        return 1 + (Tp - self.n_fft) // self.hop_length if Tp >= self.n_fft else -1
 
     def __call__(self, x, out=None):
         import torch
@@ -61,6 +74,8 @@ class MelSpectrogram:
         lead, T = tuple(x.shape[:-1]), int(x.shape[-1])
         xc = x.contiguous()
         B = xc.numel() // T if T else 0
+        if self.n_frames(T) < 1:
+            raise ValueError(f"{T} samples are too short for this framing")
         shape = (*lead, self.n_mels, self.n_frames(T))
         if out is None:
             out = torch.empty(shape, dtype=self.dtype, device=x.device)

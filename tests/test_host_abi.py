@@ -109,6 +109,30 @@ def test_plan_create_reports_unsupported(L, kw):
     assert L.fm_plan_create(C.byref(h), *args.values()) == fb.FM_ERR_UNSUPPORTED
 
 
+def _params(**kw):
+    p = dict(sr=16000, n_fft=400, hop=160, win_length=400, n_mels=80, f_min=0.0, f_max=8000.0, power=2.0,
+             mel_scale=0, norm=0, in_dtype=0, out_dtype=0, center=1, pad_mode=0, pad=0, normalized=0)
+    p.update(kw)
+    return fb.fm_plan_params(*p.values())
+
+
+@pytest.mark.parametrize("kw", [dict(pad_mode=4), dict(pad_mode=-1), dict(pad=-1), dict(pad=(1 << 20) + 1),
+                                dict(normalized=3), dict(normalized=-1), dict(n_fft=0), dict(power=-1.0)])
+def test_plan_create_ex_rejects_invalid(L, kw):
+    h = C.c_void_p(1234)
+    p = _params(**kw)
+    assert L.fm_plan_create_ex(C.byref(h), C.byref(p)) == fb.FM_ERR_INVALID_ARG
+    assert h.value is None
+    assert L.fm_plan_create_ex(C.byref(h), None) == fb.FM_ERR_INVALID_ARG
+    assert L.fm_plan_create_ex(None, C.byref(p)) == fb.FM_ERR_INVALID_ARG
+
+
+def test_plan_params_layout_matches_header():
+    # int x5, double x3, int x8 with natural alignment
+    assert C.sizeof(fb.fm_plan_params) == 5 * 4 + 4 + 3 * 8 + 8 * 4
+    assert fb.fm_plan_params.f_min.offset == 24 and fb.fm_plan_params.mel_scale.offset == 48
+
+
 def test_null_arguments(L):
     assert L.fm_plan_create(None, 16000, 400, 160, 400, 80, 0.0, 0.0, 2.0, 0, 0, 0, 0) == fb.FM_ERR_INVALID_ARG
     assert L.fm_mel_forward(None, None, 1, 1000, None, None) == fb.FM_ERR_INVALID_ARG
