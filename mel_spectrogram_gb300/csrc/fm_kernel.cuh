@@ -175,6 +175,56 @@ __device__ __forceinline__ long long padded_source(long long s, long long T, con
   return (src >= 0 && src < T) ? src : -1;
 }
 
+// The general staging path of stage_tile: rows [0, rows) of hop samples from
+// signal index gstart, in-range aligned pairs as one cp.async, every other
+// sample through padded_source. Positions from the end of the padded signal
+// (T + zpad + cpad) on are left untouched: no valid frame reads them. Kept
+// out of line: only tiles at the signal edges (or with misaligned rows) take
+// it, and its code then stays out of the kernels' hot loops.
+template <typename Raw>
+__device__ __noinline__ void stage_rows_padded(const Raw* __restrict__ src, long long T, long long gstart, int rows,
+                                               int hop, int S, Raw* dst, int warp, int nwarps, int lane,
+                                               PadSpec ps) {
+  const bool aligned = ((reinterpret_cast<uintptr_t>(src + gstart)) % (2 * sizeof(Raw))) == 0;
+  const int pairs = hop / 2;
+  const long long end = T + ps.zpad + ps.cpad;  // one past the padded signal
+  // the default framing (centre reflect, no `pad` zeros) maps by mirroring alone
+  const bool plain_reflect = ps.zpad == 0 && ps.mode == FM_PAD_REFLECT;
+  for (int r = warp; r < rows; r += nwarps) {
+    Raw* d = dst + r * S;
+    const long long s0 = gstart + (long long)r * hop;
+    if (s0 >= end) break;
+    const long long left = (end - s0 + 1) / 2;  // pairs that start inside the padded signal
+    const int c2_end = left < pairs ? (int)left : pairs;
+    for (int c2 = lane; c2 < c2_end; c2 += 32) {
+      const long long s = s0 + 2 * c2;
+      if (aligned && s >= 0 && s + 1 < T) {
+        cp_async<2 * sizeof(Raw)>(d + 2 * c2, src + s);
+        continue;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        long long se = s + e;
+        if (plain_reflect) {
+          if (se < 0) se = -se;                   // mirror about the first sample
+          else if (se >= T) se = 2 * T - 2 - se;  // mirror about the last sample
+          if (se >= T) se = -1;                   // past the padded signal (not read)
+        } else {
+          se = padded_source(se, T, ps);
+        }
+        Raw* de = d + 2 * c2 + e;
+        if (se < 0) {
+          *de = raw_zero<Raw>();
+        } else if constexpr (sizeof(Raw) == 4) {
+          cp_async<4>(de, src + se);
+        } else {
+          *de = load_one(src + se);
+        }
+      }
+    }
+  }
+}
+
 // Stage rows [0, rows) of hop samples starting at signal index gstart of
 // signal row `src` (length T) into dst (row stride S elements), as
 // asynchronous copies wherever possible: aligned in-range sample pairs as one
@@ -196,29 +246,7 @@ __device__ __forceinline__ void stage_tile(const Raw* __restrict__ src, long lon
     }
     return;
   }
-  for (int r = warp; r < rows; r += NWARPS) {
-    Raw* d = dst + r * S;
-    const long long s0 = gstart + (long long)r * hop;
-    for (int c2 = lane; c2 < pairs; c2 += 32) {
-      const long long s = s0 + 2 * c2;
-      if (aligned && s >= 0 && s + 1 < T) {
-        cp_async<2 * sizeof(Raw)>(d + 2 * c2, src + s);
-        continue;
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const long long se = padded_source(s + e, T, ps);
-        Raw* de = d + 2 * c2 + e;
-        if (se < 0) {
-          *de = raw_zero<Raw>();
-        } else if constexpr (sizeof(Raw) == 4) {
-          cp_async<4>(de, src + se);
-        } else {
-          *de = load_one(src + se);
-        }
-      }
-    }
-  }
+  stage_rows_padded<Raw>(src, T, gstart, rows, hop, S, dst, warp, NWARPS, lane, ps);
 }
 
 // Pass 1 for role p and frame g: windowed Q-point DFT of z[p + P q] and the
