@@ -71,7 +71,8 @@ typedef enum { FM_NORMALIZED_NONE = 0, FM_NORMALIZED_WINDOW = 1, FM_NORMALIZED_F
  *   out        : receives the new plan (host pointer to a pointer). Set to
  *                NULL on failure.
  *   sr         : sample rate in Hz, > 0.
- *   n_fft      : DFT size. Supported: 400 and the powers of two 64 .. 2048.
+ *   n_fft      : DFT size. Supported: 400 and the powers of two 64 .. 16384
+ *                (README "Usage": "400 or a power of 2 in [64, 16384]").
  *   hop        : frame advance in samples, > 0 and even.
  *   win_length : Hann length, 1 .. n_fft; 0 means n_fft.
  *   n_mels     : number of mel filters, 1 .. 256.

@@ -14,15 +14,17 @@
 
 #include "fm_host.h"
 #include "fm_internal.h"
+#include "fm_kernel_big.cuh"
 #include "fm_mel.h"
 
 namespace fm {
 extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant400h160, kVariant512,
-    kVariant1024, kVariant2048;
+    kVariant1024, kVariant2048, kVariant4096, kVariant8192, kVariant16384;
 
 const Variant* find_variant(int n_fft, int hop) {
-  static const Variant* all[] = {&kVariant400h160, &kVariant64,  &kVariant128,  &kVariant256, &kVariant400,
-                                 &kVariant512,     &kVariant1024, &kVariant2048};
+  static const Variant* all[] = {&kVariant400h160, &kVariant64,   &kVariant128,  &kVariant256,
+                                 &kVariant400,     &kVariant512,  &kVariant1024, &kVariant2048,
+                                 &kVariant4096,    &kVariant8192, &kVariant16384};
   for (const Variant* v : all)
     if (v->n_fft == n_fft && (v->hop == 0 || v->hop == hop)) return v;
   return nullptr;
@@ -49,6 +51,7 @@ struct fm_plan {
   float4* tw_full4;
   float2* mel_w2;
   unsigned* err;
+  float* win;        // the window, for the large-transform kernel (inside dmem)
   fm::X2Tables* x2;  // device tables of the two-frames-per-thread kernel (inside dmem)
   int x2_slots;         // its mel chunk slots
 };
@@ -264,8 +267,9 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
   const int in_esize = in_dtype == FM_F32 ? 4 : 2;
   const size_t smem_total =
-      var->kind == 1 ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize, fm::kX2Groups).total
-                     : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
+      var->kind == 1   ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize, fm::kX2Groups).total
+      : var->kind == 2 ? fm::big_smem_bytes(n_fft)
+                       : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
   if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_slots > fm::kX2MaxSlots ||
                          x2_warps > fm::kX2MaxWarps))
     return FM_ERR_UNSUPPORTED;
@@ -346,6 +350,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   const size_t o_mw2 = o;  o = fm::align16(o + sizeof(float2) * mw2.size());
   const size_t o_x2 = o;   o = fm::align16(o + (var->kind == 1 ? sizeof(fm::X2Tables) : 0));
   const size_t o_err = o;  o = fm::align16(o + sizeof(unsigned) * 4);
+  const size_t o_win = o;  o = fm::align16(o + sizeof(float) * (var->kind == 2 ? n_fft : 0));
   std::vector<unsigned char> blob(o, 0);
   if (var->kind == 1) {
     fm::X2Tables* t = reinterpret_cast<fm::X2Tables*>(blob.data() + o_x2);
@@ -366,6 +371,10 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   std::memcpy(blob.data() + o_twh4, twh4.data(), sizeof(float4) * M);
   std::memcpy(blob.data() + o_twf4, twf4.data(), sizeof(float4) * (M + 1));
   std::memcpy(blob.data() + o_mw2, mw2.data(), sizeof(float2) * mw2.size());
+  if (var->kind == 2) {  // the window with the int16 scale, for the large-transform kernel
+    float* wd = reinterpret_cast<float*>(blob.data() + o_win);
+    for (int j = 0; j < n_fft; ++j) wd[j] = win[j] * in_scale;
+  }
 
   cudaError_t e = cudaMalloc(&p->dmem, o);
   if (e != cudaSuccess) {
@@ -388,6 +397,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   p->tw_full4 = reinterpret_cast<float4*>(base + o_twf4);
   p->mel_w2 = reinterpret_cast<float2*>(base + o_mw2);
   p->err = reinterpret_cast<unsigned*>(base + o_err);
+  p->win = reinterpret_cast<float*>(base + o_win);
   p->x2 = var->kind == 1 ? reinterpret_cast<fm::X2Tables*>(base + o_x2) : nullptr;
   *out = p;
   return FM_OK;
@@ -465,6 +475,7 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.tw_full4 = plan->tw_full4;
   prm.mel_w2 = plan->mel_w2;
   prm.err = plan->err;
+  prm.win = plan->win;
 
   const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
   prm.x2 = plan->x2;

@@ -36,7 +36,7 @@ double mel_to_hz(double m, bool slaney) {
 
 bool is_supported_nfft(int n_fft) {
   if (n_fft == 400) return true;
-  for (int n = 64; n <= 2048; n *= 2)
+  for (int n = 64; n <= 16384; n *= 2)
     if (n == n_fft) return true;
   return false;
 }

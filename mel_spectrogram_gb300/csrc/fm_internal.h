@@ -46,6 +46,7 @@ struct KernelParams {
   const struct X2Tables* x2;  // two-frames-per-thread kernel only
   int x2_slots;               // its mel chunk slots (X2Tables::desc rows in use)
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
+  const float* win;       // the n_fft-point window (large-transform kernel only)
   // Packed kernel: when tmap_ok, every signal is described to the TMA unit as
   // rows of one staged line (line * in_bytes / 8 elements of 8 bytes) that
   // start at sample tmap_off + y * line, tmap_rows rows per signal, and the
@@ -191,7 +192,7 @@ struct Variant {
   int frames_per_tile;  // G: frames per tile = lanes per role
   int threads;          // P * G
   int in_buffers;       // 2: the next tile's input lands while this one computes
-  int kind;             // 0: one frame per thread; 1: two frames per thread (packed)
+  int kind;             // 0: one frame per thread; 1: two frames per thread (packed); 2: shared-memory passes
   const void* fn;       // __global__ void(KernelParams)
   int hop;              // > 0: compiled for this hop only; 0: any hop
 };

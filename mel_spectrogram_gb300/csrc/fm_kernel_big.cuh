@@ -1,0 +1,221 @@
+// Mel kernel for the large transforms (n_fft = 4096, 8192, 16384; sm_103a).
+//
+// Same path as the other kernels (padding and framing as index arithmetic,
+// periodic Hann, real DFT through the complex M = n_fft/2 point DFT of
+// z[n] = (y[2n] + i y[2n+1]) / 2 and its split, |X|^p, sparse mel projection),
+// but a frame's M complex values no longer fit one thread's registers, so the
+// complex DFT runs in shared memory as three mixed-radix autosorting
+// (Stockham) passes over a tile of F frames:
+//   load   : the windowed pairs z[n] of F consecutive frames, straight from
+//            the signal (coalesced; edge frames through padded_source);
+//   passes : radix R0, R1, R2 with M = R0 R1 R2. Pass i, with Ns the
+//            product of the earlier radices, takes the R values
+//            x[j + r M/R] of butterfly j, multiplies value r by
+//            W_{Ns R}^{(j mod Ns) r}, does an R-point DFT in registers and
+//            writes value r to x[(j / Ns) Ns R + (j mod Ns) + r Ns]; after the
+//            last pass x holds Z[k] in natural order. Every thread holds all
+//            its butterflies of a pass in registers (32 complex values), so a
+//            pass is loads, barrier, stores, barrier, in place;
+//   split  : X[k], X[M-k] from Z[k], Z[M-k] and W_N^k, |X|^p into a power
+//            tile that aliases the buffer;
+//   mel    : the CSR projection, lane = frame.
+// F = 32768 / n_fft (8, 4, 2): a tile is 16 K complex values, 139 KB of
+// shared memory with one float2 of padding per 16 (strided accesses spread
+// over the banks). Twiddles (float64-built tables) and the window are read
+// from global memory through the read-only cache.
+#pragma once
+
+#include "fm_kernel.cuh"
+
+namespace fm {
+
+constexpr int kBigThreads = 512;
+
+// Radices of the three autosorting passes, M = R0 R1 R2.
+template <int M>
+struct BigRadices;
+template <>
+struct BigRadices<2048> {
+  static constexpr int R0 = 16, R1 = 16, R2 = 8;
+};
+template <>
+struct BigRadices<4096> {
+  static constexpr int R0 = 16, R1 = 16, R2 = 16;
+};
+template <>
+struct BigRadices<8192> {
+  static constexpr int R0 = 16, R1 = 16, R2 = 32;
+};
+
+// frames per tile (F M = 16 K complex values per tile)
+__host__ __device__ constexpr int big_frames(int n_fft) { return 32768 / n_fft; }
+// float2 slots per frame in shared memory: M values, one pad per 16, one more
+__host__ __device__ constexpr int big_frame_stride(int M) { return M + (M >> 4) + 1; }
+__host__ __device__ constexpr size_t big_smem_bytes(int n_fft) {
+  return sizeof(float2) * (size_t)big_frames(n_fft) * (size_t)big_frame_stride(n_fft / 2);
+}
+__device__ __forceinline__ int big_phys(int i) { return i + (i >> 4); }
+
+__device__ __forceinline__ float raw_to_float(float v) { return v; }
+__device__ __forceinline__ float raw_to_float(short v) { return (float)v; }
+__device__ __forceinline__ float raw_to_float(__half v) { return __half2float(v); }
+
+// sample at padded position s of one signal (index arithmetic, zero where
+// padded_source says so)
+template <typename Raw>
+__device__ __forceinline__ float big_sample(const Raw* __restrict__ sig, long long T, long long s, const PadSpec& ps) {
+  const long long src = padded_source(s, T, ps);
+  return src < 0 ? 0.0f : raw_to_float(sig[src]);
+}
+
+// Windowed pairs of F frames: frame f starts at signal index s0 + f hop;
+// z[n] = (y[2n], y[2n+1]) times (w[2n], w[2n+1]) (the window carries the 1/2 of
+// the split, the STFT normalisation and the int16 scale).
+template <int N, typename Raw>
+__device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ sig, long long T, long long s0,
+                                         int hop, const float2* __restrict__ win2, const PadSpec& ps, int tid) {
+  constexpr int M = N / 2, F = big_frames(N), FS = big_frame_stride(M);
+  for (int idx = tid; idx < F * M; idx += kBigThreads) {
+    const int f = idx / M, n = idx % M;
+    const long long s = s0 + (long long)f * hop + 2 * n;
+    float a, b;
+    if (s >= 0 && s + 1 < T) {
+      a = raw_to_float(sig[s]);
+      b = raw_to_float(sig[s + 1]);
+    } else {
+      a = big_sample(sig, T, s, ps);
+      b = big_sample(sig, T, s + 1, ps);
+    }
+    const float2 w = __ldg(win2 + n);
+    s_x[f * FS + big_phys(n)] = make_float2(a * w.x, b * w.y);
+  }
+}
+
+// One radix-R autosorting pass over the F frames (Ns = product of the
+// earlier radices).
+template <int M, int F, int R, int NS>
+__device__ __forceinline__ void big_pass(float2* s_x, const float2* __restrict__ tw_m, int tid) {
+  constexpr int J = M / R;  // butterflies per frame
+  constexpr int FS = big_frame_stride(M);
+  static_assert((F * J) % kBigThreads == 0, "butterflies must divide evenly over the threads");
+  constexpr int TASKS = F * J / kBigThreads;
+  float2 v[TASKS][R];
+#pragma unroll
+  for (int t = 0; t < TASKS; ++t) {
+    const int task = tid + t * kBigThreads;
+    const int f = task / J, j = task % J;
+    const float2* xf = s_x + f * FS;
+#pragma unroll
+    for (int r = 0; r < R; ++r) v[t][r] = xf[big_phys(j + r * J)];
+    if constexpr (NS > 1) {
+      const int e = (j % NS) * (M / (NS * R));  // W_{Ns R}^{(j mod Ns) r} = W_M^{e r}, e r < M
+#pragma unroll
+      for (int r = 1; r < R; ++r) v[t][r] = cmul(v[t][r], __ldg(tw_m + e * r));
+    }
+    dft<R>(v[t]);
+  }
+  __syncthreads();  // every read of this pass before any write
+#pragma unroll
+  for (int t = 0; t < TASKS; ++t) {
+    const int task = tid + t * kBigThreads;
+    const int f = task / J, j = task % J;
+    float2* xf = s_x + f * FS;
+    const int d = (j / NS) * NS * R + (j % NS);
+#pragma unroll
+    for (int r = 0; r < R; ++r) xf[big_phys(d + r * NS)] = v[t][r];
+  }
+  __syncthreads();
+}
+
+// Real-FFT split and |X|^p for k = 0 .. M/2 of every frame, into the power
+// tile (float rows of M + 1, aliasing the buffer: all reads, barrier, writes).
+template <int M, int F, int MODE>
+__device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2* __restrict__ tw_n, float pw,
+                                          int tid) {
+  constexpr int FS = big_frame_stride(M), PS = M + 1;
+  constexpr int PAIRS = M / 2 + 1, TOTAL = F * PAIRS;
+  constexpr int PER = (TOTAL + kBigThreads - 1) / kBigThreads;
+  float lo[PER], hi[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int task = tid + i * kBigThreads;
+    lo[i] = hi[i] = 0.0f;
+    if (task < TOTAL) {
+      const int f = task / PAIRS, k = task % PAIRS;
+      const float2 zk = s_x[f * FS + big_phys(k)];
+      const float2 zm = s_x[f * FS + big_phys((M - k) & (M - 1))];
+      split_pair<MODE>(zk, zm, __ldg(tw_n + k), pw, lo[i], hi[i]);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int task = tid + i * kBigThreads;
+    if (task < TOTAL) {
+      const int f = task / PAIRS, k = task % PAIRS;
+      s_pw[f * PS + k] = lo[i];
+      s_pw[f * PS + M - k] = hi[i];
+    }
+  }
+  __syncthreads();
+}
+
+template <int N, typename Raw>
+__device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned char* smem) {
+  constexpr int M = N / 2, F = big_frames(N), NWARPS = kBigThreads / 32;
+  constexpr int R0 = BigRadices<M>::R0, R1 = BigRadices<M>::R1, R2 = BigRadices<M>::R2;
+  static_assert(R0 * R1 * R2 == M, "radices must multiply to M");
+  float2* s_x = reinterpret_cast<float2*>(smem);
+  float* s_pw = reinterpret_cast<float*>(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Raw* in = static_cast<const Raw*>(prm.in);
+  const float2* win2 = reinterpret_cast<const float2*>(prm.win);
+  const long long T = prm.T;
+  const TileSplitter split(prm.tiles_per_signal);
+  const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
+  for (long long tile = blockIdx.x; tile < prm.total_tiles; tile += gridDim.x) {
+    long long b;
+    int tt;
+    split(tile, b, tt);
+    const int t0 = tt * F;
+    __syncthreads();  // the previous tile's mel reads are done
+    big_load<N, Raw>(s_x, in + b * T, T, (long long)t0 * prm.hop - prm.lead, prm.hop, win2, pads, tid);
+    __syncthreads();
+    big_pass<M, F, R0, 1>(s_x, prm.tw_half, tid);
+    big_pass<M, F, R1, R0>(s_x, prm.tw_half, tid);
+    big_pass<M, F, R2, R0 * R1>(s_x, prm.tw_half, tid);
+    switch (prm.power_mode) {
+      case 0: big_split<M, F, 0>(s_x, s_pw, prm.tw_full, prm.power, tid); break;
+      case 1: big_split<M, F, 1>(s_x, s_pw, prm.tw_full, prm.power, tid); break;
+      default: big_split<M, F, 2>(s_x, s_pw, prm.tw_full, prm.power, tid); break;
+    }
+    const int n_valid = min(F, prm.n_frames - t0);
+    const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
+    if (prm.out_dtype == FM_F32)
+      mel_project<F, NWARPS, M + 1>(s_pw, prm.mel, prm.mel_w, static_cast<float*>(prm.out) + obase, n_valid,
+                                    prm.n_mels, prm.n_frames, warp, lane);
+    else
+      mel_project<F, NWARPS, M + 1>(s_pw, prm.mel, prm.mel_w, static_cast<__half*>(prm.out) + obase, n_valid,
+                                    prm.n_mels, prm.n_frames, warp, lane);
+  }
+}
+
+template <int N>
+__global__ void __launch_bounds__(kBigThreads, 1) mel_kernel_big(const KernelParams prm) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  pdl_launch_dependents();
+  pdl_wait();  // caller buffers only after the previous kernel in the stream is done
+  if (prm.in_dtype == FM_F32) run_tiles_big<N, float>(prm, smem);
+  else if (prm.in_dtype == FM_I16) run_tiles_big<N, short>(prm, smem);
+  else run_tiles_big<N, __half>(prm, smem);
+}
+
+}  // namespace fm
+
+// Instantiate one large-transform variant: FM_DEFINE_VARIANT_BIG(name, N)
+#define FM_DEFINE_VARIANT_BIG(NAME, N)                                                               \
+  namespace fm {                                                                                     \
+  template __global__ void mel_kernel_big<N>(const KernelParams);                                   \
+  extern const Variant NAME = {N, 0, 0, big_frames(N), kBigThreads, 0, 2,                            \
+                               (const void*)&mel_kernel_big<N>, 0};                                  \
+  }
