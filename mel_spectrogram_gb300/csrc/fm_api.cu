@@ -47,9 +47,6 @@ struct fm_plan {
   float2* tw_full;
   int4* mel;
   float* mel_w;
-  float4* tw_half4;
-  float4* tw_full4;
-  float2* mel_w2;
   unsigned* err;
   float* win;        // the window, for the large-transform kernel (inside dmem)
   fm::X2Tables* x2;  // device tables of the two-frames-per-thread kernel (inside dmem)
@@ -335,19 +332,14 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   std::vector<float4> twh4(M), twf4(M + 1);
   for (int j = 0; j < M; ++j) twh4[j] = make_float4(twh[j].x, twh[j].x, twh[j].y, twh[j].y);
   for (int j = 0; j <= M; ++j) twf4[j] = make_float4(twf[j].x, twf[j].x, twf[j].y, twf[j].y);
-  std::vector<float2> mw2(nnz > 0 ? nnz : 1);
-  for (int j = 0; j < nnz; ++j) mw2[j] = make_float2(mw[j], mw[j]);
 
-  // one device blob: p1 | tw_half | tw_full | mel | weights | err
+  // one device blob: p1 | tw_half | tw_full | mel | weights | packed-kernel tables | err | window
   size_t o = 0;
   const size_t o_p1 = o;   o = fm::align16(o + sizeof(float4) * M);
   const size_t o_twh = o;  o = fm::align16(o + sizeof(float2) * M);
   const size_t o_twf = o;  o = fm::align16(o + sizeof(float2) * (M + 1));
   const size_t o_mel = o;  o = fm::align16(o + sizeof(int4) * n_mels);
   const size_t o_mw = o;   o = fm::align16(o + sizeof(float) * (nnz > 0 ? nnz : 1));
-  const size_t o_twh4 = o; o = fm::align16(o + sizeof(float4) * M);
-  const size_t o_twf4 = o; o = fm::align16(o + sizeof(float4) * (M + 1));
-  const size_t o_mw2 = o;  o = fm::align16(o + sizeof(float2) * mw2.size());
   const size_t o_x2 = o;   o = fm::align16(o + (var->kind == 1 ? sizeof(fm::X2Tables) : 0));
   const size_t o_err = o;  o = fm::align16(o + sizeof(unsigned) * 4);
   const size_t o_win = o;  o = fm::align16(o + sizeof(float) * (var->kind == 2 ? n_fft : 0));
@@ -368,9 +360,6 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   std::memcpy(blob.data() + o_twf, twf.data(), sizeof(float2) * (M + 1));
   std::memcpy(blob.data() + o_mel, mel.data(), sizeof(int4) * n_mels);
   if (nnz > 0) std::memcpy(blob.data() + o_mw, mw.data(), sizeof(float) * nnz);
-  std::memcpy(blob.data() + o_twh4, twh4.data(), sizeof(float4) * M);
-  std::memcpy(blob.data() + o_twf4, twf4.data(), sizeof(float4) * (M + 1));
-  std::memcpy(blob.data() + o_mw2, mw2.data(), sizeof(float2) * mw2.size());
   if (var->kind == 2) {  // the window with the int16 scale, for the large-transform kernel
     float* wd = reinterpret_cast<float*>(blob.data() + o_win);
     for (int j = 0; j < n_fft; ++j) wd[j] = win[j] * in_scale;
@@ -393,9 +382,6 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   p->tw_full = reinterpret_cast<float2*>(base + o_twf);
   p->mel = reinterpret_cast<int4*>(base + o_mel);
   p->mel_w = reinterpret_cast<float*>(base + o_mw);
-  p->tw_half4 = reinterpret_cast<float4*>(base + o_twh4);
-  p->tw_full4 = reinterpret_cast<float4*>(base + o_twf4);
-  p->mel_w2 = reinterpret_cast<float2*>(base + o_mw2);
   p->err = reinterpret_cast<unsigned*>(base + o_err);
   p->win = reinterpret_cast<float*>(base + o_win);
   p->x2 = var->kind == 1 ? reinterpret_cast<fm::X2Tables*>(base + o_x2) : nullptr;
@@ -471,9 +457,6 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.tw_full = plan->tw_full;
   prm.mel = plan->mel;
   prm.mel_w = plan->mel_w;
-  prm.tw_half4 = plan->tw_half4;
-  prm.tw_full4 = plan->tw_full4;
-  prm.mel_w2 = plan->mel_w2;
   prm.err = plan->err;
   prm.win = plan->win;
 

@@ -38,11 +38,6 @@ struct KernelParams {
   const float2* tw_full;  // W_{n_fft}^k, k <= n_fft/2, stored (cos, -sin)
   const int4* mel;        // n_mels x {start, len, offset, 0}
   const float* mel_w;     // nnz
-  // the same twiddles and weights duplicated for packed (two-frame) math:
-  // {c, c, d, d} for W = c + i d, and {w, w}
-  const float4* tw_half4;
-  const float4* tw_full4;
-  const float2* mel_w2;
   const struct X2Tables* x2;  // two-frames-per-thread kernel only
   int x2_slots;               // its mel chunk slots (X2Tables::desc rows in use)
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
