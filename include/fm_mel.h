@@ -181,11 +181,20 @@ fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64_t B, int64
 /*
  * fm_mel_forward_host -- fm_mel_forward for inputs and outputs in host memory.
  *
- * Queues on `stream`: a copy of h_in [B][T] into d_in_scratch, the kernel,
- * and a copy of d_out_scratch into h_out [B][n_mels][n_frames]. The caller
- * supplies both device buffers (at least B*T and B*n_mels*n_frames elements)
- * so the call allocates nothing; pinned host memory makes the copies
- * asynchronous. The caller synchronises `stream` before reading h_out.
+ * Copies h_in [B][T] into d_in_scratch, runs the kernel and copies
+ * d_out_scratch into h_out [B][n_mels][n_frames]. The caller supplies both
+ * device buffers (at least B*T and B*n_mels*n_frames elements) so the call
+ * allocates nothing; pinned host memory makes the copies asynchronous.
+ * Ordering: the work starts after everything already queued on `stream`,
+ * and `stream` waits for all of it, so the caller synchronises `stream`
+ * before reading h_out. Inside, the signals go in up to four chunks of at
+ * least 2 MiB (input plus output bytes) through three streams that the plan
+ * owns (upload, kernel, download), so one chunk's upload overlaps another's
+ * kernel and a third's download; a call too small for two chunks runs on
+ * `stream` alone. Calls on one plan from several host threads are
+ * serialised while they queue work. Calls that share scratch buffers must
+ * be ordered by the caller, as for fm_mel_forward.
+ * The current device must be the plan's device (else FM_ERR_CUDA).
  * Errors: as fm_mel_forward, plus FM_ERR_INVALID_ARG for NULL buffers.
  */
 fm_status fm_mel_forward_host(const fm_plan* plan, const void* h_in, int64_t B, int64_t T,

@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <mutex>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -31,6 +32,19 @@ const Variant* find_variant(int n_fft, int hop) {
 }
 }  // namespace fm
 
+// Copy-in / kernel / copy-out pipeline of fm_mel_forward_host: three
+// streams and the events that chain one call's chunks; the enqueue of one
+// call holds the mutex, so calls from several host threads do not interleave
+// their use of the events.
+constexpr int kHostChunks = 4;
+constexpr size_t kHostChunkMinBytes = (size_t)2 << 20;  // input + output bytes of one chunk, at least
+struct HostPipe {
+  std::mutex mu;
+  cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t in_done[kHostChunks] = {}, comp_done[kHostChunks] = {};
+};
+
 struct fm_plan {
   int device;
   int sr, n_fft, hop, win_length, n_mels;
@@ -50,6 +64,7 @@ struct fm_plan {
   unsigned* err;
   float* win;        // the window, for the large-transform kernel (inside dmem)
   fm::X2Tables* x2;  // device tables of the two-frames-per-thread kernel (inside dmem)
+  mutable HostPipe pipe;  // streams and events of fm_mel_forward_host
   int x2_slots;         // its mel chunk slots
 };
 
@@ -182,6 +197,31 @@ fm_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return FM_OK;
   if (e == cudaErrorMemoryAllocation) return FM_ERR_OOM;
   return FM_ERR_CUDA;
+}
+
+void destroy_pipe(HostPipe& p) {
+  for (cudaStream_t* st : {&p.in, &p.comp, &p.out})
+    if (*st) cudaStreamDestroy(*st), *st = nullptr;
+  for (cudaEvent_t* ev : {&p.start, &p.end})
+    if (*ev) cudaEventDestroy(*ev), *ev = nullptr;
+  for (int i = 0; i < kHostChunks; ++i) {
+    if (p.in_done[i]) cudaEventDestroy(p.in_done[i]), p.in_done[i] = nullptr;
+    if (p.comp_done[i]) cudaEventDestroy(p.comp_done[i]), p.comp_done[i] = nullptr;
+  }
+}
+
+cudaError_t create_pipe(HostPipe& p) {
+  cudaError_t e = cudaSuccess;
+  for (cudaStream_t* st : {&p.in, &p.comp, &p.out})
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+  for (cudaEvent_t* ev : {&p.start, &p.end})
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  for (int i = 0; i < kHostChunks && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&p.in_done[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.comp_done[i], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) destroy_pipe(p);
+  return e;
 }
 
 }  // namespace
@@ -371,6 +411,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
     return from_cuda(e);
   }
   e = cudaMemcpy(p->dmem, blob.data(), o, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = create_pipe(p->pipe);
   if (e != cudaSuccess) {
     cudaFree(p->dmem);
     delete p;
@@ -392,6 +433,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
 extern "C" fm_status fm_plan_destroy(fm_plan* plan) {
   if (plan == nullptr) return FM_OK;
   cudaError_t e = cudaSuccess;
+  destroy_pipe(plan->pipe);
   if (plan->dmem) e = cudaFree(plan->dmem);
   delete plan;
   return e == cudaSuccess ? FM_OK : FM_ERR_CUDA;
@@ -487,15 +529,56 @@ extern "C" fm_status fm_mel_forward_host(const fm_plan* plan, const void* h_in, 
   fm_status st = check_forward(plan, h_in, B, T, h_out);
   if (st != FM_OK || B == 0) return st;
   if (d_in_scratch == nullptr || d_out_scratch == nullptr) return FM_ERR_INVALID_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device) return FM_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t in_bytes = (size_t)B * (size_t)T * dtype_size(plan->in_dtype);
-  const size_t out_bytes = (size_t)B * plan->n_mels * (size_t)frames_for(plan, T) * dtype_size(plan->out_dtype);
-  if (cudaMemcpyAsync(d_in_scratch, h_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return FM_ERR_CUDA;
-  st = fm_mel_forward(plan, d_in_scratch, B, T, d_out_scratch, stream);
+  const size_t in_row = (size_t)T * dtype_size(plan->in_dtype);
+  const size_t out_row = (size_t)plan->n_mels * (size_t)frames_for(plan, T) * dtype_size(plan->out_dtype);
+  const unsigned char* hin = static_cast<const unsigned char*>(h_in);
+  unsigned char* hout = static_cast<unsigned char*>(h_out);
+  unsigned char* din = static_cast<unsigned char*>(d_in_scratch);
+  unsigned char* dout = static_cast<unsigned char*>(d_out_scratch);
+  // Signals in up to kHostChunks chunks of at least kHostChunkMinBytes:
+  // copy in (pipe.in), kernel (pipe.comp), copy out (pipe.out), chained by
+  // events, so one chunk's upload, another's kernel and a third's download
+  // overlap; the three streams start after the work already queued on
+  // `stream`, which then waits for the last download. A call that makes one
+  // chunk runs on `stream` itself.
+  const int64_t C = std::min<int64_t>(
+      std::min<int64_t>(B, kHostChunks),
+      std::max<int64_t>(1, (int64_t)((size_t)B * (in_row + out_row) / kHostChunkMinBytes)));
+  if (C == 1) {
+    if (cudaMemcpyAsync(din, hin, (size_t)B * in_row, cudaMemcpyHostToDevice, s) != cudaSuccess) return FM_ERR_CUDA;
+    st = fm_mel_forward(plan, din, B, T, dout, stream);
+    if (st != FM_OK) return st;
+    if (cudaMemcpyAsync(hout, dout, (size_t)B * out_row, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return FM_ERR_CUDA;
+    return FM_OK;
+  }
+  HostPipe& P = plan->pipe;
+  std::lock_guard<std::mutex> lock(P.mu);
+  if (cudaEventRecord(P.start, s) != cudaSuccess) return FM_ERR_CUDA;
+  cudaError_t e = cudaStreamWaitEvent(P.in, P.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(P.comp, P.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(P.out, P.start, 0);
+  for (int c = 0; c < C && e == cudaSuccess && st == FM_OK; ++c) {
+    const int64_t b0 = B * c / C, nb = B * (c + 1) / C - b0;
+    e = cudaMemcpyAsync(din + b0 * in_row, hin + b0 * in_row, nb * in_row, cudaMemcpyHostToDevice, P.in);
+    if (e == cudaSuccess) e = cudaEventRecord(P.in_done[c], P.in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(P.comp, P.in_done[c], 0);
+    if (e != cudaSuccess) break;
+    st = fm_mel_forward(plan, din + b0 * in_row, nb, T, dout + b0 * out_row, reinterpret_cast<fm_stream_t>(P.comp));
+    if (st != FM_OK) break;
+    e = cudaEventRecord(P.comp_done[c], P.comp);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(P.out, P.comp_done[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(hout + b0 * out_row, dout + b0 * out_row, nb * out_row, cudaMemcpyDeviceToHost, P.out);
+  }
+  // join even after a failure, so that `stream` never runs ahead of queued work
+  cudaError_t j = cudaEventRecord(P.end, P.out);
+  if (j == cudaSuccess) j = cudaStreamWaitEvent(s, P.end, 0);
   if (st != FM_OK) return st;
-  if (cudaMemcpyAsync(h_out, d_out_scratch, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return FM_ERR_CUDA;
-  return FM_OK;
+  return (e == cudaSuccess && j == cudaSuccess) ? FM_OK : FM_ERR_CUDA;
 }
 
 extern "C" fm_status fm_plan_get_info(const fm_plan* plan, fm_plan_info* info) {

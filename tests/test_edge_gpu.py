@@ -4,6 +4,7 @@ streams, host-buffer entry point."""
 from __future__ import annotations
 
 import ctypes as C
+import dataclasses
 
 import numpy as np
 import pytest
@@ -202,6 +203,41 @@ def test_host_buffer_entry_point_matches_device_path():
                                d_out.data_ptr(), s.cuda_stream)
         s.synchronize()
         assert np.array_equal(h_out.numpy().astype(np.float64), run_gpu(w, x, plan=plan))
+    finally:
+        fb.fm_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("B", [1, 3, 5, 9])
+def test_host_buffer_entry_point_orders_with_the_stream(B):
+    """The chunked copy-in / kernel / copy-out pipeline starts after the work
+    already queued on the caller's stream and the stream waits for all of it:
+    here the input reaches its pinned host buffer through a device-to-host copy
+    queued just before the call, on a side stream, and two calls in a row
+    reuse the buffers."""
+    import torch
+
+    # 1.44 MB of input + output per signal: B = 1 runs on the caller's stream,
+    # B = 3, 5, 9 make 2, 3 and 4 chunks of uneven sizes
+    w = WORKLOADS["speech"].resized(B=B, T=200000 + 37 * B)
+    plan = plan_for(w)
+    try:
+        nf = fb.fm_n_frames(plan, w.T)
+        s = torch.cuda.Stream()
+        d_in = torch.empty((w.B, w.T), device="cuda")
+        d_out = torch.full((w.B, w.n_mels, nf), float("nan"), device="cuda")
+        h_in = torch.zeros((w.B, w.T), dtype=torch.float32).pin_memory()
+        h_out = torch.zeros((w.B, w.n_mels, nf), dtype=torch.float32).pin_memory()
+        for seed in (3, 4):
+            x = make_input(dataclasses.replace(w, seed=seed))
+            src = torch.from_numpy(x).cuda()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(s):
+                torch.cuda._sleep(2_000_000)  # the copy below lands well after the call returns
+                h_in.copy_(src, non_blocking=True)
+                fb.fm_mel_forward_host(plan, h_in.data_ptr(), w.B, w.T, h_out.data_ptr(), d_in.data_ptr(),
+                                       d_out.data_ptr(), s.cuda_stream)
+            s.synchronize()
+            assert np.array_equal(h_out.numpy().astype(np.float64), run_gpu(w, x, plan=plan)), seed
     finally:
         fb.fm_plan_destroy(plan)
 
