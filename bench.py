@@ -220,6 +220,27 @@ def run_gpu_arm(args) -> dict | None:
     clocks = clk.summary(t_start, t_end)
     assert fb.fm_plan_poll_error(plan) == fb.FM_OK
 
+    # after the timed region: five repeats of the cold-L2 replay (median) and
+    # a warm-L2 replay that reuses one input/output set (labelled as such)
+    def replay_us(g, n, reps):
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            for _ in range(reps):
+                g.replay()
+            z.record(s)
+        s.synchronize()
+        return a.elapsed_time(z) * 1e3 / (n * reps)
+
+    reps = max(1, min(K, 2000) // BUFFER_SETS)
+    repeat_us = [replay_us(graphs[BUFFER_SETS], BUFFER_SETS, reps) for _ in range(5)]
+    g_warm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=s):
+        for _ in range(BUFFER_SETS):
+            launch(0)
+    replay_us(g_warm, BUFFER_SETS, 1)
+    warm_us = replay_us(g_warm, BUFFER_SETS, reps)
+
     # end to end through the public C ABI with host buffers (copies in the region)
     Ke = max(3, min(K, args.e2e_steps))
     h_in = torch.from_numpy(x).pin_memory()
@@ -302,6 +323,11 @@ def run_gpu_arm(args) -> dict | None:
         "e2e": {"value": world * frames_step * Ke / (e_ms / 1e3), "unit": "frames/s",
                 "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b, "steps": Ke,
                 "api": "fm_mel_forward_host (pinned host buffers, copies + kernel per step)"},
+        "repeats": {"us_per_step": [round(v, 3) for v in repeat_us], "median_us": statistics.median(repeat_us),
+                    "launches_each": reps * BUFFER_SETS,
+                    "note": "cold L2 (16 rotating sets), timed after the main region"},
+        "warm_l2": {"us_per_step": warm_us, "launches": reps * BUFFER_SETS,
+                    "note": "one input/output set replayed: inputs and outputs stay in L2; not the reported value"},
         "gpu_launches": K,
         "clocks": clocks,
     }
