@@ -100,6 +100,22 @@ def make_input(w: Workload, seed: int | None = None) -> np.ndarray:
     raise ValueError(w.recipe)
 
 
+def make_input_device(w: Workload, device, seed: int | None = None):
+    """Draw a [B, T] input of workload ``w`` directly in device memory with
+    torch's seeded generator on that device (for batches too large to draw on
+    the host): normal -> float32 N(0, 1), pcm16 -> int16 uniform over
+    [-32768, 32767]. Same recipes as make_input, not the same values."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed if seed is None else seed)
+    if w.recipe == "normal":
+        return torch.randn((w.B, w.T), generator=g, device=device, dtype=torch.float32)
+    if w.recipe == "pcm16":
+        return torch.randint(-32768, 32768, (w.B, w.T), generator=g, device=device, dtype=torch.int16)
+    raise ValueError(w.recipe)
+
+
 def shard_rows(B: int, rank: int, world: int) -> tuple[int, int]:
     """Contiguous batch rows [lo, hi) owned by ``rank`` of ``world`` replicas."""
     if world <= 0 or not 0 <= rank < world:
