@@ -69,6 +69,19 @@ def recorded_traffic(workload: str):
     return float(v) if v is not None else None
 
 
+def recorded_fma_pipe(workload: str):
+    """ncu FMA-pipe utilisation (% of peak, active cycles) of the kernel, if current."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_sha") != kernel_sha():
+        return None
+    v = d.get("fma_pipe_pct", {}).get(workload)
+    return float(v) if v is not None else None
+
+
 def describe(w) -> str:
     norm = "Slaney norm" if w.norm else "no norm"
     return (f"{w.name}: B={w.B} x T={w.T} {w.in_dtype}, sr {w.sr}, n_fft {w.n_fft}, hop {w.hop}, "
@@ -319,7 +332,8 @@ def run_gpu_arm(args) -> dict | None:
         },
         "fp32": {"achieved_tflops": flops / step_s / 1e12, "peak_tflops": fp32_peak,
                  "frac": flops / step_s / 1e12 / fp32_peak,
-                 "peak_basis": f"{props.multi_processor_count} SMs x 128 lanes x 2 x {clk_mhz:.0f} MHz"},
+                 "peak_basis": f"{props.multi_processor_count} SMs x 128 lanes x 2 x {clk_mhz:.0f} MHz",
+                 "ncu_fma_pipe_pct": recorded_fma_pipe(w.name)},
         "e2e": {"value": world * frames_step * Ke / (e_ms / 1e3), "unit": "frames/s",
                 "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b, "steps": Ke,
                 "api": "fm_mel_forward_host (pinned host buffers, copies + kernel per step)"},
