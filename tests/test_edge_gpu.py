@@ -242,6 +242,78 @@ def test_host_buffer_entry_point_orders_with_the_stream(B):
         fb.fm_plan_destroy(plan)
 
 
+def test_host_buffer_entry_point_in_a_cuda_graph():
+    """The plan's three streams fork from and join the capturing stream, so a
+    multi-chunk call records into a CUDA graph whose replays recompute h_out."""
+    import torch
+
+    w = WORKLOADS["speech"].resized(B=4, T=480000)
+    plan = plan_for(w)
+    try:
+        nf = fb.fm_n_frames(plan, w.T)
+        x1, x2 = make_input(w), make_input(dataclasses.replace(w, seed=9))
+        h_in = torch.from_numpy(x1).pin_memory()
+        h_out = torch.zeros((w.B, w.n_mels, nf), dtype=torch.float32).pin_memory()
+        d_in = torch.empty((w.B, w.T), device="cuda")
+        d_out = torch.empty((w.B, w.n_mels, nf), device="cuda")
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fb.fm_mel_forward_host(plan, h_in.data_ptr(), w.B, w.T, h_out.data_ptr(), d_in.data_ptr(),
+                                   d_out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        for x in (x1, x2):
+            h_in.copy_(torch.from_numpy(x))
+            g.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(h_out.numpy().astype(np.float64), run_gpu(w, x, plan=plan))
+    finally:
+        fb.fm_plan_destroy(plan)
+
+
+def test_host_buffer_entry_point_from_two_threads():
+    """Calls on one plan from two host threads, each with its own stream and
+    buffers: the plan serialises their queuing and every result is right."""
+    import threading
+
+    import torch
+
+    w = WORKLOADS["speech"].resized(B=3, T=300000)
+    plan = plan_for(w)
+    nf = fb.fm_n_frames(plan, w.T)
+    xs = [make_input(dataclasses.replace(w, seed=20 + i)) for i in range(2)]
+    want = [run_gpu(w, x, plan=plan) for x in xs]
+    errors = []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            h_in = torch.from_numpy(xs[i]).pin_memory()
+            h_out = torch.zeros((w.B, w.n_mels, nf), dtype=torch.float32).pin_memory()
+            d_in = torch.empty((w.B, w.T), device="cuda")
+            d_out = torch.empty((w.B, w.n_mels, nf), device="cuda")
+            for _ in range(20):
+                h_out.zero_()
+                fb.fm_mel_forward_host(plan, h_in.data_ptr(), w.B, w.T, h_out.data_ptr(), d_in.data_ptr(),
+                                       d_out.data_ptr(), s.cuda_stream)
+                s.synchronize()
+                if not np.array_equal(h_out.numpy().astype(np.float64), want[i]):
+                    errors.append(f"thread {i}: wrong output")
+                    return
+        except Exception as e:  # reported below
+            errors.append(f"thread {i}: {e!r}")
+
+    try:
+        ts = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        assert not errors, errors
+    finally:
+        fb.fm_plan_destroy(plan)
+
+
 def test_plan_info():
     w = WORKLOADS["speech"]
     plan = plan_for(w)
