@@ -186,6 +186,47 @@ def test_side_stream_and_transform_module():
     mel.close()
 
 
+def test_transform_module_refusals_dtypes_and_empty_batch():
+    """MelSpectrogram refuses what it cannot compute (autograd input, float64,
+    a signal too short to reflect, a mismatched out=) and runs int16 / f16
+    inputs, f16 output and an empty batch through the same C-ABI path."""
+    import torch
+
+    from mel_spectrogram_gb300 import MelSpectrogram
+
+    w = WORKLOADS["tiny"].resized(B=2, T=4003)
+    mel = MelSpectrogram(sample_rate=16000, n_fft=400, hop_length=160, n_mels=80, f_max=8000.0)
+    mel16 = MelSpectrogram(sample_rate=16000, n_fft=400, hop_length=160, n_mels=80, f_max=8000.0,
+                           dtype=torch.float16)
+    try:
+        x = torch.from_numpy(make_input(w)).cuda().requires_grad_(True)
+        with pytest.raises(RuntimeError):
+            mel(x)
+        with torch.no_grad():
+            y = mel(x)
+        check_close(y.double().cpu().numpy(), oracle_for(w, make_input(w)), "f32", "no_grad input")
+        with pytest.raises(TypeError):
+            mel(torch.zeros(2, 4000, dtype=torch.float64, device="cuda"))
+        with pytest.raises(fb.FmError):
+            mel(torch.zeros(1, 200, device="cuda"))  # reflect padding needs T > n_fft / 2
+        with pytest.raises(ValueError):
+            mel(x.detach(), out=torch.empty(2, 80, 10, device="cuda"))
+        for tag, recipe in (("i16", "pcm16"), ("f16", "music16")):
+            wt = dataclasses.replace(w, in_dtype=tag, recipe=recipe)
+            xt = make_input(wt)
+            got = mel(torch.from_numpy(xt).cuda()).double().cpu().numpy()
+            check_close(got, oracle_for(wt, xt), "f32", f"module {tag} input")
+        xf = make_input(w)
+        got16 = mel16(torch.from_numpy(xf).cuda())
+        assert got16.dtype == torch.float16
+        check_close(got16.double().cpu().numpy(), oracle_for(w, xf), "f16", "module f16 output")
+        y0 = mel(torch.zeros(0, 4003, device="cuda"))
+        assert tuple(y0.shape) == (0, 80, 26)
+    finally:
+        mel.close()
+        mel16.close()
+
+
 def test_host_buffer_entry_point_matches_device_path():
     import torch
 
