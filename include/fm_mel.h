@@ -239,6 +239,34 @@ fm_status fm_mel_forward_host_noalloc(const fm_plan* plan, const void* h_in, int
                                       void* h_out, fm_stream_t stream);
 
 /*
+ * fm_selftest_wait_timeout -- diagnostic: runs out, on purpose, one of the
+ * bounded waits of the kernels, so that the timeout path can be exercised
+ * without faulting or hanging the GPU. The pages have no counterpart
+ * (flashmel's kernels have no device-side waits).
+ *
+ * One CTA of two groups of 64 threads; each group waits, with the kernels'
+ * own wait code and exit vote, on its own mbarrier for 2^log2_polls polls.
+ * Group 1's barrier completes by an arrival; nothing arrives on group 0's, so
+ * group 0 gives up, records FM_ERR_KERNEL_TIMEOUT in the plan's error word
+ * (read it with fm_plan_poll_error, as after a real kernel) and leaves, while
+ * group 1 finishes normally. The call synchronises `stream`.
+ *   kind            : 0 = a tile group's wait for its staged tile (blocking
+ *                     mbarrier.try_wait polls); 1 = the producer warp's wait
+ *                     for a free staging area (non-blocking test_wait polls
+ *                     with a short sleep between them).
+ *   log2_polls      : 0 .. the kernels' own limit for that wait.
+ *   groups_completed: host int, may be NULL; receives the number of groups
+ *                     that passed their wait (1 when the path works).
+ *   elapsed_us      : host double, may be NULL; the kernel's duration by CUDA
+ *                     events, from which the time per poll follows.
+ * Calls are serialised within the process; the plan must be on the current
+ * device. Errors: FM_ERR_INVALID_ARG for a NULL plan, another kind or
+ * log2_polls out of range; FM_ERR_CUDA if a CUDA call fails.
+ */
+fm_status fm_selftest_wait_timeout(const fm_plan* plan, int kind, int log2_polls, fm_stream_t stream,
+                                   int* groups_completed, double* elapsed_us);
+
+/*
  * fm_mel_filterbank_csr -- the plan's filterbank, computed on the host only
  * (no CUDA call), for inspection and tests.
  *

@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     fm_plan_destroy,
     fm_plan_get_info,
     fm_plan_poll_error,
+    fm_selftest_wait_timeout,
     lib,
     status_string,
 )

@@ -32,6 +32,7 @@ EXPORTS = [
     "fm_plan_get_info",
     "fm_plan_poll_error",
     "fm_status_string",
+    "fm_selftest_wait_timeout",
 ]
 
 
@@ -97,6 +98,8 @@ def lib() -> C.CDLL:
     L.fm_plan_poll_error.restype = ci
     L.fm_status_string.argtypes = [ci]
     L.fm_status_string.restype = C.c_char_p
+    L.fm_selftest_wait_timeout.argtypes = [vp, ci, ci, vp, C.POINTER(ci), C.POINTER(cd)]
+    L.fm_selftest_wait_timeout.restype = ci
     _lib = L
     return L
 
@@ -170,6 +173,20 @@ def fm_mel_forward_host(plan, h_in: int, B: int, T: int, h_out: int, d_in: int, 
 
 # size of the device staging array of fm_mel_forward_host_noalloc (FM_NOALLOC_MAX_BYTES)
 FM_NOALLOC_MAX_BYTES = 32 << 20
+
+
+def fm_selftest_wait_timeout(plan, kind: int, log2_polls: int, stream: int = 0) -> tuple[int, float]:
+    """Run out one of the kernels' bounded waits on purpose (diagnostic).
+
+    kind 0: a tile group's wait for its staged tile; kind 1: the producer
+    warp's wait for a free staging area. Returns (groups that passed their
+    wait, kernel microseconds); the timeout itself is then reported by
+    fm_plan_poll_error.
+    """
+    done, us = C.c_int(0), C.c_double(0.0)
+    _check(lib().fm_selftest_wait_timeout(plan, int(kind), int(log2_polls), stream or None, C.byref(done),
+                                          C.byref(us)), "fm_selftest_wait_timeout")
+    return done.value, us.value
 
 
 def fm_mel_forward_host_noalloc(plan, h_in: int, B: int, T: int, h_out: int, stream: int = 0) -> None:

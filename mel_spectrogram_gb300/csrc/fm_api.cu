@@ -604,6 +604,8 @@ extern "C" fm_status fm_plan_get_info(const fm_plan* plan, fm_plan_info* info) {
   return FM_OK;
 }
 
+unsigned* fm::plan_error_word(const fm_plan* plan) { return plan ? plan->err : nullptr; }
+
 extern "C" fm_status fm_plan_poll_error(const fm_plan* plan) {
   if (plan == nullptr) return FM_ERR_INVALID_ARG;
   unsigned word = 0;

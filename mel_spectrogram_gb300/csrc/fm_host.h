@@ -27,4 +27,8 @@ void build_window(int n_fft, int win_length, int normalized, std::vector<float>&
 // tw[j] = exp(-2 pi i j / len), j < count, stored (cos, -sin).
 void build_twiddles(int len, int count, std::vector<float2>& tw);
 
+// The plan's device error word (the one fm_plan_poll_error reads), for the
+// diagnostic kernels of the library; NULL for a NULL plan.
+unsigned* plan_error_word(const fm_plan* plan);
+
 }  // namespace fm

@@ -111,14 +111,32 @@ __device__ __forceinline__ bool mbar_test_wait(unsigned long long* bar, unsigned
       : "memory");
   return ok != 0;
 }
-// Bounded wait for phase `parity` of an mbarrier. Gives up after ~2^22 polls
-// (far longer than any copy), records FM_ERR_KERNEL_TIMEOUT in *err and
-// returns false, so a lost transfer never hangs the GPU.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, unsigned parity, unsigned* err) {
-  for (int i = 0; i < (1 << 22); ++i)
+// Bounded wait for phase `parity` of an mbarrier: gives up after `polls`
+// try_wait polls, records FM_ERR_KERNEL_TIMEOUT in *err and returns false, so
+// a lost transfer never hangs the GPU.
+__device__ __forceinline__ bool mbar_wait_polls(unsigned long long* bar, unsigned parity, unsigned* err, int polls) {
+  for (int i = 0; i < polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   if (err) atomicExch(err, (unsigned)FM_ERR_KERNEL_TIMEOUT);
   return false;
+}
+// The kernels' wait for a staged tile: 2^18 try_wait polls. A poll that finds
+// the phase incomplete suspends the thread for about 3.8 us on GB300
+// (measured), so the wait gives up after about a second, some 10^4 times
+// longer than any staged copy takes.
+constexpr int kWaitLog2Polls = 18;
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, unsigned parity, unsigned* err) {
+  return mbar_wait_polls(bar, parity, err, 1 << kWaitLog2Polls);
+}
+// Back-off of a polling loop built on non-blocking tests (the producer warp's
+// wait for a free staging area): sleeps briefly and returns true while the
+// loop has been idle for at most `polls` rounds, false once it should give up.
+// 2^22 rounds of about 100 ns (measured on GB300) give up after ~0.4 s.
+constexpr int kIdleLog2Polls = 22;
+__device__ __forceinline__ bool idle_backoff(int& idle, int polls) {
+  if (++idle > polls) return false;
+  __nanosleep(32);
+  return true;
 }
 
 // Programmatic dependent launch: let the next kernel in the stream start its

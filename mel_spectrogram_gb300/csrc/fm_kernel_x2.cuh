@@ -344,11 +344,10 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     ready = __shfl_sync(0xffffffffu, ready, 0);
     if (!left) break;
     if (ready < 0) {
-      if (++idle > (1 << 22)) {
+      if (!idle_backoff(idle, 1 << kIdleLog2Polls)) {
         if (lane == 0) atomicExch(prm.err, (unsigned)FM_ERR_KERNEL_TIMEOUT);
         break;
       }
-      __nanosleep(32);
       continue;
     }
     idle = 0;
