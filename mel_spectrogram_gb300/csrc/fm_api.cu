@@ -310,10 +310,15 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_slots > fm::kX2MaxSlots ||
                          x2_warps > fm::kX2MaxWarps))
     return FM_ERR_UNSUPPORTED;
-  if (smem_total > (size_t)prop.sharedMemPerBlockOptin) return FM_ERR_UNSUPPORTED;
+  // the kernel's static shared memory comes out of the same per-block limit
+  cudaFuncAttributes fattr;
+  if (cudaFuncGetAttributes(&fattr, var->fn) != cudaSuccess) return FM_ERR_CUDA;
+  const size_t dyn_max = prop.sharedMemPerBlockOptin > fattr.sharedSizeBytes
+                             ? prop.sharedMemPerBlockOptin - fattr.sharedSizeBytes
+                             : 0;
+  if (smem_total > dyn_max) return FM_ERR_UNSUPPORTED;
   // allow the device maximum once, so plans of different sizes never undercut each other
-  if (cudaFuncSetAttribute(var->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)prop.sharedMemPerBlockOptin) != cudaSuccess)
+  if (cudaFuncSetAttribute(var->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_max) != cudaSuccess)
     return FM_ERR_CUDA;
   int bps = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, var->fn, var->threads, smem_total) != cudaSuccess)

@@ -46,6 +46,14 @@ __device__ __forceinline__ void cp_async(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(d), "l"(gsrc), "n"(BYTES) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// Make mbarrier `bar` track this thread's cp.async copies issued so far: its
+// pending count goes up by one now and comes down (an arrival) once they have
+// landed, so a waiter on the phase sees the copied bytes without the issuing
+// thread blocking on them.
+__device__ __forceinline__ void cp_async_mbar_arrive(unsigned long long* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"((unsigned)__cvta_generic_to_shared(bar))
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 // ---------------------------------------------------------------------------

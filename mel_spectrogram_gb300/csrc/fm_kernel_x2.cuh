@@ -250,6 +250,31 @@ struct X2Staging {
   }
 };
 
+// Lines [r0, r1) of a staged tile (line r starts at signal index
+// gstart + r L) under the default framing, centre reflect padding with no
+// `pad` zeros: sample s comes from -s before the signal, s inside it and
+// 2 T - 2 - s in the cpad samples after it; positions from T + cpad on are
+// left untouched (no valid frame reads them). One warp, 32-bit offsets within
+// the lines, each sample by one 4-byte cp.async (f32 only).
+template <typename Raw>
+__device__ __forceinline__ void stage_lines_reflect(const Raw* __restrict__ sig, long long T, long long gstart,
+                                                    int r0, int r1, int L, int S, int cpad, Raw* dst, int lane) {
+  const long long base = gstart + (long long)r0 * L;
+  const int n = (r1 - r0) * L;
+  const auto clamp_n = [n](long long v) { return (int)(v < 0 ? 0 : (v > n ? n : v)); };
+  const int a = clamp_n(-base);           // i < a: before the signal
+  const int b = clamp_n(T - base);        // a <= i < b: inside it
+  const int c = clamp_n(T + cpad - base);  // b <= i < c: mirrored after it
+  for (int r = 0, i0 = 0; r < r1 - r0 && i0 < c; ++r, i0 += L) {
+    Raw* d = dst + (r0 + r) * S;
+    for (int col = lane; col < L && i0 + col < c; col += 32) {
+      const int i = i0 + col;
+      const long long src = i < a ? -(base + i) : (i < b ? base + i : 2 * T - 2 - (base + i));
+      cp_async<4>(d + col, sig + src);
+    }
+  }
+}
+
 // The producer warp: stages every tile of the CTA's groups into the group's
 // staging area (the upper half of its exchange buffer). Lines that lie inside
 // the signal arrive by TMA bulk copies, one line per lane, when the signal's
@@ -257,9 +282,11 @@ struct X2Staging {
 // "staged" mbarrier. The other lines (the reflect-padded edges, or every line
 // of an unaligned signal) are gathered by the warp's lanes with cp.async
 // element copies, mirrored about the first / last sample; lines that start
-// past the padded signal are skipped (no valid frame reads them). Lane 0 then
-// arrives on the mbarrier, so its phase completes once both kinds of copies
-// have landed. A group's next tile is staged once the group reports its
+// past the padded signal are skipped (no valid frame reads them). Every lane
+// hands its element copies to the mbarrier (cp.async.mbarrier.arrive: a
+// pending arrival that lands with them) and lane 0 then arrives, so the phase
+// completes once both kinds of copies have landed while the warp already
+// serves the next group. A group's next tile is staged once the group reports its
 // staging area free (its "free" mbarrier, after pass 2 has read the exchange
 // buffer); the warp serves whichever group is ready first. Waits are bounded:
 // if no group frees its area for ~2^22 polls the warp records
@@ -275,6 +302,14 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
   const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
   unsigned long long* full = reinterpret_cast<unsigned long long*>(smem + lay.bars);
   unsigned long long* empty = full + kX2Groups;
+  // The tensor map's rows are lines of L samples starting at signal index
+  // tmap_off, and lead + tmap_off is a multiple of L, so tile tt's first line
+  // is tensor row tt * kX2Frames / KH - y_lead.
+  const int y_lead = (prm.lead + prm.tmap_off) / st.line;
+  // the default framing (centre reflect, no `pad` zeros) with f32 samples; its
+  // edge tiles take stage_lines_reflect (16-bit samples keep stage_tile's
+  // pairwise cp.async)
+  const bool plain_reflect = sizeof(Raw) == 4 && prm.zpad == 0 && prm.pad_mode == FM_PAD_REFLECT;
   auto stage = [&](int g, long long tile) {
     long long b;
     int tt;
@@ -282,21 +317,24 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     const long long gstart = (long long)tt * kX2Frames * st.hop - prm.lead;
     const Raw* sig = in + b * T;
     Raw* dst = reinterpret_cast<Raw*>(smem + lay.in_tile + g * lay.group_stride);
-    const long long L = st.line;
+    const int L = st.line, rows = st.rows;
+    const long long span = (long long)rows * L;
     // lines [r_lo, r_hi) lie inside [0, T); lines from r_end on start past
-    // the padded signal (T + zpad + cpad)
-    long long r_lo = gstart >= 0 ? 0 : (-gstart + L - 1) / L;
-    long long r_hi = (T - gstart) / L;
-    long long r_end = (T + prm.zpad + prm.cpad - gstart + L - 1) / L;
-    r_end = r_end < st.rows ? r_end : st.rows;
+    // the padded signal (T + zpad + cpad). Clamped to the tile's rows, every
+    // count fits 32 bits, so no 64-bit division is needed.
+    int r_lo = gstart >= 0 ? 0 : ((int)(-gstart) + L - 1) / L;  // -gstart <= lead
+    const long long avail = T - gstart;
+    int r_hi = avail >= span ? rows : (avail <= 0 ? 0 : (int)avail / L);
+    const long long avail_p = T + prm.zpad + prm.cpad - gstart;
+    const int r_end = avail_p >= span ? rows : (avail_p <= 0 ? 0 : ((int)avail_p + L - 1) / L);
     r_hi = r_hi < r_end ? r_hi : r_end;
-    const bool tma_ok = ((st.line * esize) & 15) == 0 && (reinterpret_cast<uintptr_t>(sig + gstart) & 15) == 0;
+    const bool tma_ok = ((L * esize) & 15) == 0 && (reinterpret_cast<uintptr_t>(sig + gstart) & 15) == 0;
     if (!tma_ok || r_lo >= r_hi) r_lo = r_hi = 0;
     // an interior tile whose rows all lie in the tensor map: one tensor copy
-    const long long y0 = (gstart - prm.tmap_off) / L;
-    const bool one_copy = prm.tmap_ok && gstart >= prm.tmap_off && y0 + st.rows <= prm.tmap_rows &&
-                          (smem_addr(dst) & 127u) == 0;
-    if (one_copy) r_lo = r_hi = r_end = 0;
+    const int y0 = tt * (kX2Frames / X2Staging<N, HOP, Raw>::KH) - y_lead;
+    const bool one_copy = prm.tmap_ok && y0 >= 0 && y0 + rows <= prm.tmap_rows && (smem_addr(dst) & 127u) == 0;
+    int r_stop = r_end;
+    if (one_copy) r_lo = r_hi = r_stop = 0;
     // the consumers' generic accesses of the area were ordered before this
     // warp by the "free" mbarrier; order them before the async-proxy writes
     if (lane == 0) {
@@ -309,16 +347,28 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
       }
     }
     __syncwarp();
-    for (int r = (int)r_lo + lane; r < (int)r_hi; r += 32)
-      tma_load_1d(dst + r * st.S, sig + gstart + r * L, (unsigned)(L * esize), full + g);
-    if (r_lo > 0) stage_tile<Raw, 1>(sig, T, gstart, (int)r_lo, st.line, st.S, dst, 0, lane, pads);
-    const int r_tail = (int)(r_hi > r_lo ? r_hi : r_lo);
-    if (r_end > r_tail)
-      stage_tile<Raw, 1>(sig, T, gstart + r_tail * L, (int)r_end - r_tail, st.line, st.S, dst + r_tail * st.S, 0,
-                         lane, pads);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncwarp();  // every lane's element copies have landed
+    for (int r = r_lo + lane; r < r_hi; r += 32)
+      tma_load_1d(dst + r * st.S, sig + gstart + (long long)r * L, (unsigned)(L * esize), full + g);
+    const int r_tail = r_hi > r_lo ? r_hi : r_lo;
+    // a tile that reaches past an edge of the signal mirrors its padding with
+    // stage_lines_reflect; the others keep stage_tile's pairwise copies
+    const bool mirror = plain_reflect && (gstart < 0 || avail < span);
+    if constexpr (sizeof(Raw) == 4) {
+      if (mirror) {
+        if (r_lo > 0) stage_lines_reflect<Raw>(sig, T, gstart, 0, r_lo, L, st.S, prm.cpad, dst, lane);
+        if (r_stop > r_tail) stage_lines_reflect<Raw>(sig, T, gstart, r_tail, r_stop, L, st.S, prm.cpad, dst, lane);
+      }
+    }
+    if (!mirror) {
+      if (r_lo > 0) stage_tile<Raw, 1>(sig, T, gstart, r_lo, L, st.S, dst, 0, lane, pads);
+      if (r_stop > r_tail)
+        stage_tile<Raw, 1>(sig, T, gstart + (long long)r_tail * L, r_stop - r_tail, L, st.S, dst + r_tail * st.S,
+                           0, lane, pads);
+    }
+    // each lane's element copies arrive on the group's barrier when they land,
+    // so the warp goes on to the next group instead of waiting for DRAM here
+    cp_async_mbar_arrive(full + g);
+    __syncwarp();  // every lane's pending arrival is registered before lane 0's
     if (lane == 0) mbar_arrive(full + g);
   };
   int next_k[kX2Groups];
@@ -355,6 +405,7 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     stage(ready, x2_tile(ready, next_k[ready]));
     ++next_k[ready];
   }
+  cp_async_wait_all();  // no copy of this warp stays in flight past its exit
 }
 
 // The tile loop of one group (P x 16 threads on named barrier 1 + grp, its
