@@ -509,6 +509,25 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
 
   const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
   prm.x2 = plan->x2;
+  // two-frames-per-thread kernel: move the signals' first and last tiles (the
+  // slow ones to stage) into the third group's first slots, when there are at
+  // most as many as CTAs and every slot they take holds an interior tile
+  prm.perm_edges = 0;
+  prm.perm_t0 = 0;
+  if (v->kind == 1) {
+    const long long tps = prm.tiles_per_signal, n_edge = 2 * B, t0 = (long long)(fm::kX2Groups - 1) * grid;
+    if (tps >= 3 && n_edge <= grid && t0 + n_edge <= prm.total_tiles) {
+      bool ok = true;
+      for (long long i = 0; i < n_edge && ok; ++i) {
+        const long long tt = (t0 + i) % tps;
+        ok = tt != 0 && tt != tps - 1;
+      }
+      if (ok) {
+        prm.perm_edges = (int)n_edge;
+        prm.perm_t0 = t0;
+      }
+    }
+  }
   encode_input_map(plan, d_in, B, T, prm);
   void* args[] = {&prm};
   // programmatic dependent launch: the kernel waits (griddepcontrol.wait) for

@@ -29,6 +29,11 @@ struct KernelParams {
   float power;
   int tiles_per_signal;
   long long total_tiles;
+  // two-frames-per-thread kernel: slots [perm_t0, perm_t0 + perm_edges) take
+  // the signals' first and last tiles and those tiles' slots take the tiles
+  // displaced (0: every slot processes its own tile)
+  int perm_edges;
+  long long perm_t0;
   // pass-1 table, one float4 per (role p, q) at [p * Q + q]: the window at
   // samples 2n and 2n+1 (n = p + P q, times 1/2 for the real-FFT split and
   // times 2^-15 for int16 input) and, as int bits, the offset of sample 2n in
@@ -137,9 +142,11 @@ __host__ __device__ inline int in_row_stride_x2(int len, int esize) { return in_
 // appended).
 struct SmemLayoutX2 {
   // group g's "tile staged" mbarrier at bars + 8 g and its "staging area free"
-  // mbarrier at bars + 8 (groups + g); its exchange buffer at
-  // xbuf + g group_stride and its staged tile at in_tile + g group_stride
-  size_t bars, p1, tw_half, tw_full, desc, w4, xbuf, in_tile, in_tile_bytes, group_stride, total;
+  // mbarrier at bars + 8 (groups + g); the (signal, tile in signal) of its
+  // k-th tile at slots + 8 (2 g + k % 2), written by the producer; its
+  // exchange buffer at xbuf + g group_stride and its staged tile at
+  // in_tile + g group_stride
+  size_t bars, slots, p1, tw_half, tw_full, desc, w4, xbuf, in_tile, in_tile_bytes, group_stride, total;
 };
 
 // Staged lines of the packed kernel: k_hops hops of samples per line (2 for
@@ -156,7 +163,8 @@ __host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int k
   const int ns = n_slots > 0 ? n_slots : 1;
   SmemLayoutX2 L;
   size_t o = 0;
-  L.bars = o;      o = align16(o + sizeof(unsigned long long) * 2 * groups);
+  L.bars = o;      o = o + sizeof(unsigned long long) * 2 * groups;
+  L.slots = o;     o = align16(o + sizeof(int2) * 2 * groups);
   L.p1 = o;        o = align16(o + sizeof(float4) * M);
   L.tw_half = o;   o = align16(o + sizeof(float4) * M);
   L.tw_full = o;   o = align16(o + sizeof(float4) * (M + 1));

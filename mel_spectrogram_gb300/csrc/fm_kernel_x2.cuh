@@ -236,6 +236,25 @@ __device__ __forceinline__ long long x2_tile(int g, int k) {
   return (long long)blockIdx.x + (long long)gridDim.x * (g + (long long)kX2Groups * k);
 }
 
+// The tile that slot p processes. A signal's first and last tiles take
+// padding and are the slowest to stage; the host may swap them (perm_edges)
+// with interior tiles of the slots [perm_t0, perm_t0 + perm_edges), which it
+// sets to the third group's first tiles: that group has the fewest tiles, so
+// a late start costs it nothing, and no later round then waits behind an
+// edge tile. Edge tile 2b is signal b's first, 2b + 1 its last.
+__device__ __forceinline__ long long x2_logical(const KernelParams& prm, const TileSplitter& split, long long p) {
+  if (prm.perm_edges == 0) return p;
+  const long long i = p - prm.perm_t0;
+  const long long tps = prm.tiles_per_signal;
+  if (i >= 0 && i < prm.perm_edges) return (i >> 1) * tps + (i & 1) * (tps - 1);
+  long long b;
+  int tt;
+  split(p, b, tt);
+  if (tt == 0) return prm.perm_t0 + 2 * b;
+  if (tt == tps - 1) return prm.perm_t0 + 2 * b + 1;
+  return p;
+}
+
 // Geometry of the staged tile: lines of KH hops (two for a compile-time hop,
 // else one), `rows` lines with a stride of S samples.
 template <int N, int HOP, typename Raw>
@@ -310,10 +329,12 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
   // edge tiles take stage_lines_reflect (16-bit samples keep stage_tile's
   // pairwise cp.async)
   const bool plain_reflect = sizeof(Raw) == 4 && prm.zpad == 0 && prm.pad_mode == FM_PAD_REFLECT;
-  auto stage = [&](int g, long long tile) {
+  int2* slots = reinterpret_cast<int2*>(smem + lay.slots);
+  auto stage = [&](int g, long long tile, int k) {
     long long b;
     int tt;
     split(tile, b, tt);
+    if (lane == 0) slots[2 * g + (k & 1)] = make_int2((int)b, tt);  // published by the arrival below
     const long long gstart = (long long)tt * kX2Frames * st.hop - prm.lead;
     const Raw* sig = in + b * T;
     Raw* dst = reinterpret_cast<Raw*>(smem + lay.in_tile + g * lay.group_stride);
@@ -378,7 +399,7 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     phase[g] = 0u;
     next_k[g] = 0;
     if (x2_tile(g, 0) < prm.total_tiles) {
-      stage(g, x2_tile(g, 0));
+      stage(g, x2_logical(prm, split, x2_tile(g, 0)), 0);
       next_k[g] = 1;
     }
   }
@@ -402,7 +423,7 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     }
     idle = 0;
     phase[ready] ^= 1u;
-    stage(ready, x2_tile(ready, next_k[ready]));
+    stage(ready, x2_logical(prm, split, x2_tile(ready, next_k[ready])), next_k[ready]);
     ++next_k[ready];
   }
   cp_async_wait_all();  // no copy of this warp stays in flight past its exit
@@ -445,7 +466,6 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
   const unsigned char* s_pw = s_x;
   float2* pw_col = reinterpret_cast<float2*>(s_x) + 2 * (g & 7) + (g >> 3);
   const X2Staging<N, HOP, Raw> st(prm.hop);
-  const TileSplitter split(prm.tiles_per_signal);
   const int s_begin = __ldg(&prm.x2->warp_begin[warp]), s_end = __ldg(&prm.x2->warp_begin[warp + 1]);
   const Raw* s_in = reinterpret_cast<const Raw*>(smem + lay.in_tile + grp * lay.group_stride);
   // frame g's first sample (HOP > 0: plus 2p, the role's first pair)
@@ -497,9 +517,11 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
     }
     group_sync(bar_id, THREADS);
 
-    long long b;
-    int tt;
-    split(tile, b, tt);
+    // the tile's place, as the producer staged it (slot k % 2 is rewritten
+    // only for tile k + 2, after this group has freed its area twice more)
+    const int2 bt = reinterpret_cast<const int2*>(smem + lay.slots)[2 * grp + (k & 1)];
+    const long long b = bt.x;
+    const int tt = bt.y;
     const int t0 = tt * kX2Frames;
     const int n_valid = min(kX2Frames, prm.n_frames - t0);
     const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
