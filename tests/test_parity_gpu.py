@@ -48,3 +48,17 @@ def test_workload_parity_full_size_sampled_rows(name):
     for b in sorted({0, w.B // 2 + 1, w.B - 1}):
         ref = oracle_for(w.resized(B=1), x[b : b + 1])
         check_close(got[b : b + 1], ref, w.out_dtype, f"{name}[b={b}]")
+
+
+@pytest.mark.parametrize("B,in_dtype,recipe", [(4, "f32", "normal"), (5, "i16", "pcm16")])
+def test_edge_tiles_moved_to_spare_slots(B, in_dtype, recipe):
+    """Batches large enough that the packed kernel runs every signal's first
+    and last tile in the third tile group's first slots (more than three tile
+    rounds of 152 CTAs), compared element by element with the oracle."""
+    import dataclasses
+
+    w = dataclasses.replace(WORKLOADS["speech"].resized(B=B, T=480000 + 37), in_dtype=in_dtype, recipe=recipe)
+    tiles = B * -(-(1 + w.T // w.hop) // 32)
+    assert tiles >= 2 * 152 + 2 * B  # room for the swap on a 152-SM part
+    x = make_input(w)
+    check_close(run_gpu(w, x), oracle_for(w, x), w.out_dtype, f"B={B} {in_dtype}")
