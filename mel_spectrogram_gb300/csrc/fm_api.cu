@@ -4,10 +4,10 @@
 
 #include <algorithm>
 #include <climits>
-#include <mutex>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -598,8 +598,17 @@ extern "C" fm_status fm_mel_forward_host(const fm_plan* plan, const void* h_in, 
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(hout + b0 * out_row, dout + b0 * out_row, nb * out_row, cudaMemcpyDeviceToHost, P.out);
   }
-  // join even after a failure, so that `stream` never runs ahead of queued work
-  cudaError_t j = cudaEventRecord(P.end, P.out);
+  // join even after a failure, so that `stream` never runs ahead of queued
+  // work; after one, an upload or kernel may be queued that no download
+  // follows, so the download stream first waits for the other two
+  cudaError_t j = cudaSuccess;
+  if (e != cudaSuccess || st != FM_OK) {
+    j = cudaEventRecord(P.in_done[0], P.in);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(P.out, P.in_done[0], 0);
+    if (j == cudaSuccess) j = cudaEventRecord(P.comp_done[0], P.comp);
+    if (j == cudaSuccess) j = cudaStreamWaitEvent(P.out, P.comp_done[0], 0);
+  }
+  if (j == cudaSuccess) j = cudaEventRecord(P.end, P.out);
   if (j == cudaSuccess) j = cudaStreamWaitEvent(s, P.end, 0);
   if (st != FM_OK) return st;
   return (e == cudaSuccess && j == cudaSuccess) ? FM_OK : FM_ERR_CUDA;
