@@ -278,6 +278,7 @@ struct X2Staging {
 template <typename Raw>
 __device__ __forceinline__ void stage_lines_reflect(const Raw* __restrict__ sig, long long T, long long gstart,
                                                     int r0, int r1, int L, int S, int cpad, Raw* dst, int lane) {
+  static_assert(sizeof(Raw) == 4, "4-byte samples only");
   const long long base = gstart + (long long)r0 * L;
   const int n = (r1 - r0) * L;
   const auto clamp_n = [n](long long v) { return (int)(v < 0 ? 0 : (v > n ? n : v)); };
