@@ -140,6 +140,14 @@ def test_null_arguments(L):
     assert L.fm_n_frames(None, 100) == -1
     assert L.fm_plan_get_info(None, None) == fb.FM_ERR_INVALID_ARG
     assert L.fm_plan_poll_error(None) == fb.FM_ERR_INVALID_ARG
+    # the host-buffer entry points and the diagnostic refuse a missing plan
+    # before any CUDA call
+    assert L.fm_mel_forward_host(None, None, 1, 1000, None, None, None, None) == fb.FM_ERR_INVALID_ARG
+    assert L.fm_mel_forward_host_noalloc(None, None, 1, 1000, None, None) == fb.FM_ERR_INVALID_ARG
+    done, us = C.c_int(-1), C.c_double(-1.0)
+    for kind in (0, 1, 2):
+        assert L.fm_selftest_wait_timeout(None, kind, 4, None, C.byref(done), C.byref(us)) == fb.FM_ERR_INVALID_ARG
+    assert done.value == -1 and us.value == -1.0  # nothing written on refusal
     nnz = C.c_int64(0)
     assert L.fm_mel_filterbank_csr(16000, 400, 80, 0.0, 0.0, 0, 0, None, None, None, None, None) == \
         fb.FM_ERR_INVALID_ARG
