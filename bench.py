@@ -336,7 +336,8 @@ def run_gpu_arm(args) -> dict | None:
                  "ncu_fma_pipe_pct": recorded_fma_pipe(w.name)},
         "e2e": {"value": world * frames_step * Ke / (e_ms / 1e3), "unit": "frames/s",
                 "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b, "steps": Ke,
-                "api": "fm_mel_forward_host (pinned host buffers, copies + kernel per step)"},
+                "api": "fm_mel_forward_host (pinned host buffers; per step the upload, kernel and download "
+                       "of up to four signal chunks, overlapped on plan-owned streams)"},
         "repeats": {"us_per_step": [round(v, 3) for v in repeat_us], "median_us": statistics.median(repeat_us),
                     "launches_each": reps * BUFFER_SETS,
                     "note": "cold L2 (16 rotating sets), timed after the main region"},
