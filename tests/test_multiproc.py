@@ -83,3 +83,17 @@ def test_two_rank_replicas_match_single_process(tmp_path):
     assert full.shape == ref.shape
     assert np.array_equal(full, ref)
     assert float(np.load(tmp_path / "tmax.npy")[0]) == float(world)
+
+
+def test_reference_arm_runs_on_rank_zero_only(tmp_path):
+    """Under torchrun the oracle arm of bench.py runs and prints on rank 0
+    alone; any other rank exits 0 without work or output."""
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "3",
+                        "--warmup", "3", "--workload", "tiny"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
