@@ -57,7 +57,9 @@ def test_wait_runs_out_and_is_reported_then_the_context_still_works(kind):
         print(f"\nwait kind {kind}: {per_poll * 1e3:.1f} ns per poll; the kernels' limit gives up after "
               f"{give_up:.2f} s; times {times}")
         assert times[12] > times[4]
-        assert 0.05 < give_up < 3.0, "the kernels' wait limit should be about a second"
+        # the poll time is the hardware's (3.8 us per blocking poll on GB300 so
+        # far); the bound only rules out a limit far from a second
+        assert 0.01 < give_up < 5.0, "the kernels' wait limit should be about a second"
     finally:
         fb.fm_plan_destroy(plan)
 
