@@ -133,6 +133,38 @@ def test_plan_params_layout_matches_header():
     assert fb.fm_plan_params.f_min.offset == 24 and fb.fm_plan_params.mel_scale.offset == 48
 
 
+def _c_layout(struct: str, fields: list[str], tmp_path) -> dict:
+    """sizeof and offsetof of a struct from include/fm_mel.h, as the C compiler
+    lays it out (a small program compiled with the host's cc)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("cc") or shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "fm_mel.h"', 'int main(void) {',
+             f'  printf("size %zu\\n", sizeof({struct}));']
+    lines += [f'  printf("{f} %zu\\n", offsetof({struct}, {f}));' for f in fields]
+    lines += ['  return 0;', '}']
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(root, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    return {k: int(v) for k, v in (ln.split() for ln in out.splitlines())}
+
+
+@pytest.mark.parametrize("name", ["fm_plan_params", "fm_plan_info"])
+def test_binding_structs_match_the_c_layout(name, tmp_path):
+    cls = getattr(fb, name)
+    fields = [f for f, _ in cls._fields_]
+    got = _c_layout(name, fields, tmp_path)
+    assert got["size"] == C.sizeof(cls)
+    for f in fields:
+        assert got[f] == getattr(cls, f).offset, f
+
+
 def test_null_arguments(L):
     assert L.fm_plan_create(None, 16000, 400, 160, 400, 80, 0.0, 0.0, 2.0, 0, 0, 0, 0) == fb.FM_ERR_INVALID_ARG
     assert L.fm_mel_forward(None, None, 1, 1000, None, None) == fb.FM_ERR_INVALID_ARG
