@@ -33,6 +33,48 @@ def test_header_declares_what_the_binding_exports():
     assert declared_functions() == sorted(fb.EXPORTS)
 
 
+def declared_prototypes() -> dict[str, tuple[str, list[str]]]:
+    """name -> (return type, parameter types) of every function in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w ]*?\**)\s+\**(fm_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", text):
+        types = []
+        for prm in params.split(","):
+            prm = " ".join(prm.split())
+            if not prm or prm == "void":
+                continue
+            # drop the parameter name, keep the type with its stars
+            types.append(re.sub(r"\s*\b\w+$", "", prm).replace("const ", "").strip())
+        out[name] = (ret.replace("const ", "").strip(), types)
+    return out
+
+
+def _ctype_for(t: str):
+    """The ctypes type the binding must use for a C parameter type."""
+    if t.endswith("*") or t == "fm_stream_t":
+        return "pointer"
+    return {"int": C.c_int, "int64_t": C.c_int64, "double": C.c_double, "fm_status": C.c_int,
+            "fm_mel_scale": C.c_int, "fm_norm": C.c_int, "fm_dtype": C.c_int}[t]
+
+
+def test_binding_signatures_match_the_header(L):
+    protos = declared_prototypes()
+    assert sorted(protos) == declared_functions()
+    for name, (ret, params) in protos.items():
+        fn = getattr(L, name)
+        assert len(fn.argtypes) == len(params), name
+        for i, (t, a) in enumerate(zip(params, fn.argtypes)):
+            want = _ctype_for(t)
+            if want == "pointer":
+                assert a is C.c_void_p or a is C.c_char_p or issubclass(a, C._Pointer), (name, i, t, a)
+            else:
+                assert a is want, (name, i, t, a)
+        if ret.endswith("*"):
+            assert fn.restype in (C.c_char_p, C.c_void_p), name
+        else:
+            assert fn.restype is _ctype_for(ret), (name, ret, fn.restype)
+
+
 def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
