@@ -197,6 +197,29 @@ def _c_layout(struct: str, fields: list[str], tmp_path) -> dict:
     return {k: int(v) for k, v in (ln.split() for ln in out.splitlines())}
 
 
+def test_binding_constants_match_the_header(tmp_path):
+    """Every FM_* constant the binding defines has the header's value (the C
+    compiler evaluates the header's enums and macros)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("cc") or shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [n for n in dir(fb) if n.startswith("FM_") and isinstance(getattr(fb, n), int)]
+    assert len(names) >= 20
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    body = "\n".join(f'  printf("{n} %lld\\n", (long long)({n}));' for n in names)
+    src = tmp_path / "consts.c"
+    src.write_text('#include <stdio.h>\n#include "fm_mel.h"\nint main(void) {\n' + body + "\n  return 0;\n}\n")
+    exe = tmp_path / "consts"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(root, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {k: int(v) for k, v in (ln.split() for ln in out.splitlines())}
+    for n in names:
+        assert got[n] == getattr(fb, n), n
+
+
 @pytest.mark.parametrize("name", ["fm_plan_params", "fm_plan_info"])
 def test_binding_structs_match_the_c_layout(name, tmp_path):
     cls = getattr(fb, name)
