@@ -1,6 +1,6 @@
 """Helpers for the GPU tests: run the C-ABI path, compare with the oracle.
 
-Tolerances (stated by the benchmark spec, applied element by element):
+Tolerances (the bounds the path is held to, applied element by element):
   fp32 output: |gpu - oracle| <= 1e-4 * (1 + |oracle|)
   f16 output : |gpu - oracle| <= 2e-3 * (1 + |oracle|) everywhere, and
                <= 2e-3 * |oracle| wherever |oracle| >= 6.1e-5 (f16 normals)
