@@ -3,7 +3,6 @@ parameters, every element written, exact dtype conversions, alignment,
 streams, host-buffer entry point."""
 from __future__ import annotations
 
-import ctypes as C
 import dataclasses
 
 import numpy as np

@@ -8,7 +8,6 @@ a CPU tensor) before any CUDA call.
 """
 from __future__ import annotations
 
-import itertools
 
 import numpy as np
 import pytest

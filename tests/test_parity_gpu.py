@@ -6,7 +6,6 @@ times) are checked on whole sampled signals.
 """
 from __future__ import annotations
 
-import numpy as np
 import pytest
 
 from mel_spectrogram_gb300.workloads import ORDER, WORKLOADS, make_input
