@@ -72,3 +72,25 @@ def test_defaults_follow_torchaudio(win_length, hop_length):
     assert mel.win_length == win
     assert mel.hop_length == (win // 2 if hop_length is None else hop_length)
     assert mel.f_max == 22050 / 2 and mel.n_mels == 128 and mel.power == 2.0
+
+
+def test_device_input_generator_recipes():
+    """make_input_device (the generator of the batches past 2^31 samples)
+    follows the recipes' dtype and range, is seeded, and refuses the others;
+    on the CPU here, torch's generator being the same code on any device."""
+    import dataclasses
+
+    import torch
+
+    from mel_spectrogram_gb300.workloads import WORKLOADS, make_input_device
+
+    w = WORKLOADS["int16"].resized(B=2, T=50000)
+    a, b = make_input_device(w, "cpu"), make_input_device(w, "cpu")
+    assert a.dtype == torch.int16 and tuple(a.shape) == (2, 50000)
+    assert torch.equal(a, b)  # seeded
+    assert int(a.min()) < -30000 and int(a.max()) > 30000  # the full int16 range
+    assert not torch.equal(a, make_input_device(w, "cpu", seed=99))
+    s = make_input_device(WORKLOADS["speech"].resized(B=1, T=100000), "cpu")
+    assert s.dtype == torch.float32 and abs(float(s.mean())) < 0.02 and abs(float(s.std()) - 1.0) < 0.02
+    with pytest.raises(ValueError):
+        make_input_device(dataclasses.replace(w, recipe="music16"), "cpu")
