@@ -187,6 +187,108 @@ def _uncentred_frame_count(o):
     o.n_frames_uncentred = lambda T, n_fft, hop: 1 + (T - n_fft + hop - 1) // hop
 
 
+def _slaney_linear_slope(o):
+    orig_h2m, orig_m2h = o.hz_to_mel, o.mel_to_hz
+
+    def h2m(f, scale):
+        if scale == "slaney":
+            f = np.asarray(f, dtype=np.float64)
+            return np.where(f >= 1000.0, orig_h2m(f, scale), f / 100.0)  # 10 mels per kHz instead of 15
+        return orig_h2m(f, scale)
+
+    def m2h(m, scale):
+        if scale == "slaney":
+            m = np.asarray(m, dtype=np.float64)
+            return np.where(m >= 15.0, orig_m2h(m, scale), 100.0 * m)
+        return orig_m2h(m, scale)
+
+    o.hz_to_mel, o.mel_to_hz = h2m, m2h
+
+
+def _slaney_log10(o):
+    orig = o.hz_to_mel
+
+    def h2m(f, scale):
+        if scale == "slaney":
+            f = np.asarray(f, dtype=np.float64)
+            log = 15.0 + 27.0 * np.log10(np.maximum(f, 1e-300) / 1000.0) / np.log10(6.4) * 0.5  # half the step
+            return np.where(f >= 1000.0, log, f / (200.0 / 3.0))
+        return orig(f, scale)
+
+    o.hz_to_mel = h2m
+
+
+def _vertices_one_short(o):
+    def fv(f_min, f_max, n_mels, scale):
+        m = np.linspace(o.hz_to_mel(f_min, scale), o.hz_to_mel(f_max, scale), n_mels + 1)
+        m = np.append(m, m[-1] + (m[-1] - m[-2]))  # n_mels + 1 steps squeezed, last vertex past f_max
+        return o.mel_to_hz(m, scale)
+
+    o.filter_vertices = fv
+
+
+def _bin_grid_coarse(o):
+    o.bin_frequencies = lambda n_fft, sr: np.arange(n_fft // 2 + 1, dtype=np.float64) * (float(sr) / (n_fft - 2))
+
+
+def _window_left_aligned(o):
+    def hann(win_length, n_fft):
+        n = np.arange(win_length, dtype=np.float64)
+        out = np.zeros(n_fft)
+        out[:win_length] = 0.5 - 0.5 * np.cos(2.0 * math.pi * n / win_length)  # not centred
+        return out
+
+    o.hann_periodic = hann
+
+
+def _frames_one_late(o):
+    def frame(xp, n_fft, hop, count):
+        idx = np.arange(count)[:, None] * hop + np.arange(n_fft)[None, :] + 1
+        idx = np.minimum(idx, xp.shape[-1] - 1)
+        return xp[..., idx]
+
+    o.frame = frame
+
+
+def _power_ignored(o):
+    orig = o.spectral_power
+    o.spectral_power = lambda X, power: orig(X, 2.0)
+
+
+def _frame_length_norm_by_win(o):
+    orig = o.window_norm
+
+    def wn(w, n_fft, normalized):
+        if normalized == "frame_length":
+            return 1.0 / math.sqrt(float(np.count_nonzero(w)) + 1.0)  # the window's support, not n_fft
+        return orig(w, n_fft, normalized)
+
+    o.window_norm = wn
+
+
+def _constant_pads_edge(o):
+    orig = o.centre_pad
+
+    def cp(x, pad, mode):
+        if mode == "constant" and pad > 0:
+            return orig(x, pad, "replicate")
+        return orig(x, pad, mode)
+
+    o.centre_pad = cp
+
+
+def _f_max_ignored(o):
+    orig = o.mel_filterbank
+    o.mel_filterbank = lambda n_fft, sr, n_mels, f_min, f_max, scale="htk", norm=None: orig(
+        n_fft, sr, n_mels, f_min, sr / 2.0, scale, norm)
+
+
+def _f_min_ignored(o):
+    orig = o.mel_filterbank
+    o.mel_filterbank = lambda n_fft, sr, n_mels, f_min, f_max, scale="htk", norm=None: orig(
+        n_fft, sr, n_mels, 0.0, f_max, scale, norm)
+
+
 MUTANTS = [
     _symmetric_hann,
     _edge_repeating_pad,
@@ -202,6 +304,17 @@ MUTANTS = [
     _zero_pad_after_centring,
     _window_norm_linear_sum,
     _uncentred_frame_count,
+    _slaney_linear_slope,
+    _slaney_log10,
+    _vertices_one_short,
+    _bin_grid_coarse,
+    _window_left_aligned,
+    _frames_one_late,
+    _power_ignored,
+    _frame_length_norm_by_win,
+    _constant_pads_edge,
+    _f_max_ignored,
+    _f_min_ignored,
 ]
 
 
