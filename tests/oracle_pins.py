@@ -244,6 +244,24 @@ def check_filterbank_shape(o):
         assert np.all(F[:, ~cover].sum(axis=0) <= 1.0 + 1e-12)
 
 
+def check_band_limits(o):
+    """The filterbank spans exactly the band [f_min, f_max]: its first
+    triangle starts at f_min and its last ends at f_max, so on the bin grid
+    k sr / n_fft every weight at or below f_min, or at or above f_max, is
+    zero, and the bins strictly inside the band carry weight."""
+    for n_fft, sr, n_mels, f_min, f_max, scale in [
+        (512, 16000, 40, 125.0, 7600.0, "slaney"),
+        (1024, 16000, 64, 300.0, 3400.0, "htk"),
+        (2048, 44100, 96, 40.0, 15000.0, "slaney"),
+    ]:
+        F = o.mel_filterbank(n_fft, sr, n_mels, f_min, f_max, scale, None)
+        fk = np.arange(n_fft // 2 + 1) * sr / n_fft
+        outside = (fk <= f_min) | (fk >= f_max)
+        assert np.all(F[:, outside] == 0.0), (n_fft, f_min, f_max)
+        inside = ~outside
+        assert np.all(F[:, inside].sum(axis=0) > 0.0), (n_fft, f_min, f_max)
+
+
 def check_slaney_area(o):
     """With Slaney norm every triangle has unit area (Riemann sum over bins)."""
     sr = 22050
@@ -324,4 +342,5 @@ ALL_CHECKS = [
     check_torch_stft,
     check_framing_brute_force,
     check_window_normalisation,
+    check_band_limits,
 ]
