@@ -289,6 +289,56 @@ def _f_min_ignored(o):
         n_fft, sr, n_mels, 0.0, f_max, scale, norm)
 
 
+def _int16_unsigned(o):
+    orig = o.to_float64
+
+    def conv(x):
+        x = np.asarray(x)
+        if x.dtype == np.int16:
+            return x.view(np.uint16).astype(np.float64) / 32768.0  # sign bit read as magnitude
+        return orig(x)
+
+    o.to_float64 = conv
+
+
+def _reflect_right_repeats_edge(o):
+    orig = o.reflect_pad
+
+    def rp(x, pad):
+        out = orig(x, pad)
+        if pad > 0:
+            T = x.shape[-1]
+            out[..., pad + T :] = x[..., T - pad :][..., ::-1]  # right mirror repeats x[T-1]
+        return out
+
+    o.reflect_pad = rp
+
+
+def _htk_break_1000(o):
+    orig_h2m, orig_m2h = o.hz_to_mel, o.mel_to_hz
+
+    def h2m(f, scale):
+        if scale == "htk":
+            return 2595.0 * np.log10(1.0 + np.asarray(f, dtype=np.float64) / 1000.0)
+        return orig_h2m(f, scale)
+
+    def m2h(m, scale):
+        if scale == "htk":
+            return 1000.0 * (10.0 ** (np.asarray(m, dtype=np.float64) / 2595.0) - 1.0)
+        return orig_m2h(m, scale)
+
+    o.hz_to_mel, o.mel_to_hz = h2m, m2h
+
+
+def _filters_reversed(o):
+    orig = o.mel_filterbank
+    o.mel_filterbank = lambda *a, **k: orig(*a, **k)[::-1].copy()
+
+
+def _normalized_ignored(o):
+    o.window_norm = lambda w, n_fft, normalized: 1.0
+
+
 MUTANTS = [
     _symmetric_hann,
     _edge_repeating_pad,
@@ -315,6 +365,11 @@ MUTANTS = [
     _constant_pads_edge,
     _f_max_ignored,
     _f_min_ignored,
+    _int16_unsigned,
+    _reflect_right_repeats_edge,
+    _htk_break_1000,
+    _filters_reversed,
+    _normalized_ignored,
 ]
 
 
