@@ -262,6 +262,28 @@ def check_band_limits(o):
         assert np.all(F[:, inside].sum(axis=0) > 0.0), (n_fft, f_min, f_max)
 
 
+def check_shift_and_scale(o):
+    """Two invariants of the transform. Shift: advancing the signal by one hop
+    moves every frame that reads no padding up by one (frame t + 1 of x is
+    frame t of x[hop:]). Homogeneity: scaling the signal by a scales the
+    output by a^p, for the power p."""
+    rng = np.random.default_rng(17)
+    for n_fft, hop, power in [(400, 160, 2.0), (256, 64, 1.0), (512, 200, 0.5)]:
+        T = 12 * n_fft + 37
+        x = rng.standard_normal((1, T))
+        args = (16000, n_fft, hop, 40, 0.0, 8000.0, power, "htk", None)
+        full = o.mel_spectrogram(x, *args)[0]
+        moved = o.mel_spectrogram(x[:, hop:], *args)[0]
+        half = n_fft // 2
+        t_lo = -(-half // hop)  # first frame of x[hop:] that starts inside it
+        t_hi = (T - hop - half) // hop  # last frame of x[hop:] that ends inside it
+        assert t_hi - t_lo > 5
+        np.testing.assert_allclose(moved[:, t_lo : t_hi + 1], full[:, t_lo + 1 : t_hi + 2], rtol=1e-9, atol=1e-9)
+        a = 3.0
+        scaled = o.mel_spectrogram(a * x, *args)[0]
+        np.testing.assert_allclose(scaled, a ** power * full, rtol=1e-9, atol=1e-12)
+
+
 def check_slaney_area(o):
     """With Slaney norm every triangle has unit area (Riemann sum over bins)."""
     sr = 22050
@@ -343,4 +365,5 @@ ALL_CHECKS = [
     check_framing_brute_force,
     check_window_normalisation,
     check_band_limits,
+    check_shift_and_scale,
 ]
