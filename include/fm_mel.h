@@ -55,9 +55,10 @@ typedef enum { FM_F32 = 0, FM_I16 = 1, FM_F16 = 2 } fm_dtype;
 /* torch's pad modes for the centre padding: mirror without repeating the
  * edge sample, zeros, repeat the edge sample, wrap around the signal */
 typedef enum { FM_PAD_REFLECT = 0, FM_PAD_CONSTANT = 1, FM_PAD_REPLICATE = 2, FM_PAD_CIRCULAR = 3 } fm_pad_mode;
-/* STFT normalisation, folded into the window: none, divide by
- * sqrt(sum w^2) (torchaudio normalized=True / "window"), or by sqrt(n_fft)
- * ("frame_length", torch.stft normalized=True) */
+/* STFT normalisation, folded into the window (flashmel filters.py
+ * make_window): none, divide by sqrt(sum w^2) (normalized=True / "window"),
+ * or by sqrt(win_length) ("frame_length"; torch.stft's sqrt(n_fft) when
+ * win_length = n_fft) */
 typedef enum { FM_NORMALIZED_NONE = 0, FM_NORMALIZED_WINDOW = 1, FM_NORMALIZED_FRAME_LENGTH = 2 } fm_normalized;
 
 /*

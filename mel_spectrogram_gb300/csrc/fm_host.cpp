@@ -97,7 +97,8 @@ void build_filterbank(int sr, int n_fft, int n_mels, double f_min, double f_max,
 
 void build_window(int n_fft, int win_length, int normalized, std::vector<float>& window) {
   // periodic Hann of win_length samples, zero-padded and centred in n_fft;
-  // times the STFT normalisation (1, 1/sqrt(sum w^2) or 1/sqrt(n_fft)) and
+  // times the STFT normalisation (1, 1/sqrt(sum w^2) or 1/sqrt(win_length),
+  // flashmel filters.py make_window) and
   // times 1/2, the factor of the real-FFT split that the kernel leaves out.
   window.assign(n_fft, 0.0f);
   const int left = (n_fft - win_length) / 2;
@@ -109,7 +110,7 @@ void build_window(int n_fft, int win_length, int normalized, std::vector<float>&
   }
   double scale = 1.0;
   if (normalized == FM_NORMALIZED_WINDOW) scale = 1.0 / std::sqrt(energy);
-  else if (normalized == FM_NORMALIZED_FRAME_LENGTH) scale = 1.0 / std::sqrt((double)n_fft);
+  else if (normalized == FM_NORMALIZED_FRAME_LENGTH) scale = 1.0 / std::sqrt((double)win_length);
   for (int n = 0; n < win_length; ++n) window[left + n] = (float)(0.5 * scale * w[n]);
 }
 

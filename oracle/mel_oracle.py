@@ -43,7 +43,9 @@ page only names torchaudio's ``melscale_fbanks``):
     signal; without centring, frames start at sample 0 and there are
     1 + floor((T - n_fft) / hop) of them;
   * normalized "window" (or True) divides the spectrum by sqrt(sum w^2),
-    "frame_length" by sqrt(n_fft) (torch.stft's normalisation).
+    "frame_length" by sqrt(win_length) (flashmel README, filters.py
+    make_window: the window divided by the square root of its own length;
+    equal to torch.stft's sqrt(n_fft) whenever win_length = n_fft).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, Parseval, filterbank invariants).
@@ -203,15 +205,15 @@ def spectral_power(X: np.ndarray, power: float) -> np.ndarray:
     return mag2 ** (power / 2.0)
 
 
-def window_norm(w: np.ndarray, n_fft: int, normalized) -> float:
-    """Scale folded into the window: 1, 1/sqrt(sum w^2) ("window" or True),
-    or 1/sqrt(n_fft) ("frame_length")."""
+def window_norm(w: np.ndarray, win_length: int, normalized) -> float:
+    """Scale folded into the window (filters.py make_window): 1,
+    1/sqrt(sum w^2) ("window" or True), or 1/sqrt(win_length) ("frame_length")."""
     if normalized in (False, None, "none"):
         return 1.0
     if normalized in (True, "window"):
         return 1.0 / math.sqrt(float(np.sum(w * w)))
     if normalized == "frame_length":
-        return 1.0 / math.sqrt(n_fft)
+        return 1.0 / math.sqrt(win_length)
     raise ValueError(normalized)
 
 
@@ -238,7 +240,7 @@ def power_spectrogram(
         count = n_frames_uncentred(T, n_fft, hop)
     frames = frame(xp, n_fft, hop, count)
     w = hann_periodic(win_length, n_fft)
-    y = frames * (w * window_norm(w, n_fft, normalized))
+    y = frames * (w * window_norm(w, win_length, normalized))
     P = spectral_power(dft_onesided(y), power)
     return np.swapaxes(P, -1, -2)
 

@@ -92,7 +92,7 @@ def brute_power_framed(x, n_fft, hop, win_length, power, center, pad_mode, pad, 
     if normalized in (True, "window"):
         scale = 1.0 / math.sqrt(sum(v * v for v in w))
     elif normalized == "frame_length":
-        scale = 1.0 / math.sqrt(n_fft)
+        scale = 1.0 / math.sqrt(win_length)
     else:
         scale = 1.0
     frames = 1 + T // hop if center else 1 + (T - n_fft) // hop
@@ -304,7 +304,8 @@ def check_input_conversion(o):
 def check_torch_stft(o):
     """Library special case: torch.stft, float64, periodic Hann, centre reflect
     and every other framing torch offers (pad modes, no centring, `pad` zeros
-    first as torchaudio applies them, frame-length normalisation)."""
+    first as torchaudio applies them, frame-length normalisation rescaled
+    from torch's sqrt(n_fft) to the page's sqrt(win_length))."""
     import torch
     import torch.nn.functional as tf
 
@@ -328,7 +329,9 @@ def check_torch_stft(o):
                 for normalized in (False, True):
                     S = torch.stft(xt, n_fft, hop, win, window=w, center=center, pad_mode=mode,
                                    normalized=normalized, return_complex=True)
-                    ref = (S.abs() ** 2).numpy()
+                    # torch.stft's normalized=True divides by sqrt(n_fft), the
+                    # page's frame-length normalisation by sqrt(win_length)
+                    ref = (S.abs() ** 2).numpy() * (n_fft / win if normalized else 1.0)
                     got = o.power_spectrogram(x, n_fft, hop, win, 2.0, center, mode, zp,
                                               "frame_length" if normalized else False)
                     assert got.shape == ref.shape, (mode, center, got.shape, ref.shape)
@@ -337,14 +340,15 @@ def check_torch_stft(o):
 
 def check_window_normalisation(o):
     """An impulse inside a frame gives |X[k]| = w[j] / sqrt(sum w^2) for every
-    k with the window normalisation (the frame-length one: w[j] / sqrt(N))."""
+    k with the window normalisation, and w[j] / sqrt(win_length) with the
+    frame-length one (flashmel filters.py make_window)."""
     n_fft, hop, T, n0, win = 64, 16, 400, 211, 50
     x = np.zeros(T)
     x[n0] = 1.0
     lpad = (n_fft - win) // 2
     w = np.zeros(n_fft)
     w[lpad : lpad + win] = [0.5 - 0.5 * math.cos(2.0 * math.pi * n / win) for n in range(win)]
-    for normalized, scale in (("window", 1.0 / math.sqrt(float(np.dot(w, w)))), ("frame_length", 1.0 / 8.0)):
+    for normalized, scale in (("window", 1.0 / math.sqrt(float(np.dot(w, w)))), ("frame_length", 1.0 / math.sqrt(win))):
         P = o.power_spectrogram(x, n_fft, hop, win, 1.0, True, "reflect", 0, normalized)
         for t in range(P.shape[1]):
             j = n0 + n_fft // 2 - t * hop

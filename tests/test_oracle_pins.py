@@ -166,7 +166,7 @@ def _zero_pad_after_centring(o):
             count = o.n_frames_uncentred(T, n_fft, hop)
         frames = o.frame(xp, n_fft, hop, count)
         w = o.hann_periodic(win_length, n_fft)
-        return np.swapaxes(o.spectral_power(o.dft_onesided(frames * w * o.window_norm(w, n_fft, normalized)), power),
+        return np.swapaxes(o.spectral_power(o.dft_onesided(frames * w * o.window_norm(w, win_length, normalized)), power),
                            -1, -2)
 
     o.power_spectrogram = ps
@@ -175,10 +175,10 @@ def _zero_pad_after_centring(o):
 def _window_norm_linear_sum(o):
     orig = o.window_norm
 
-    def wn(w, n_fft, normalized):
+    def wn(w, win_length, normalized):
         if normalized in (True, "window"):
             return 1.0 / float(np.sum(w))
-        return orig(w, n_fft, normalized)
+        return orig(w, win_length, normalized)
 
     o.window_norm = wn
 
@@ -255,13 +255,13 @@ def _power_ignored(o):
     o.spectral_power = lambda X, power: orig(X, 2.0)
 
 
-def _frame_length_norm_by_win(o):
+def _frame_length_norm_by_nfft(o):
     orig = o.window_norm
 
-    def wn(w, n_fft, normalized):
+    def wn(w, win_length, normalized):
         if normalized == "frame_length":
-            return 1.0 / math.sqrt(float(np.count_nonzero(w)) + 1.0)  # the window's support, not n_fft
-        return orig(w, n_fft, normalized)
+            return 1.0 / math.sqrt(float(w.shape[-1]))  # the frame (torch.stft), not the window's length
+        return orig(w, win_length, normalized)
 
     o.window_norm = wn
 
@@ -336,7 +336,7 @@ def _filters_reversed(o):
 
 
 def _normalized_ignored(o):
-    o.window_norm = lambda w, n_fft, normalized: 1.0
+    o.window_norm = lambda w, win_length, normalized: 1.0
 
 
 MUTANTS = [
@@ -361,7 +361,7 @@ MUTANTS = [
     _window_left_aligned,
     _frames_one_late,
     _power_ignored,
-    _frame_length_norm_by_win,
+    _frame_length_norm_by_nfft,
     _constant_pads_edge,
     _f_max_ignored,
     _f_min_ignored,
