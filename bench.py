@@ -27,10 +27,10 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from mel_spectrogram_gb300.workloads import WORKLOADS, make_input  # noqa: E402
+from mel_spectrogram_gb300.workloads import ORDER, WORKLOADS, make_input  # noqa: E402
 
-METRIC = "mel frames/sec and achieved HBM GB/s (fraction of roofline) at B=8×480000 fp32"
 BUFFER_SETS = 16
+HOST_SLACK_CYCLES = 200_000  # ~0.1 ms of device-side wait ahead of a timed region
 L2_BYTES = 129 * 1024 * 1024
 def kernel_sha() -> str:
     """Fingerprint of the device code (every kernel source and header)."""
@@ -159,6 +159,139 @@ def dist_env():
     return world, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def metric_for(w) -> str:
+    """The metric string for workload ``w`` (the headline names the speech batch)."""
+    return (f"mel frames/sec and achieved HBM GB/s (fraction of roofline) at B={w.B}×{w.T} "
+            f"{ {'f32': 'fp32', 'i16': 'int16', 'f16': 'f16'}[w.in_dtype] }")
+
+
+class WorkloadRun:
+    """One workload's plan, rotating device buffers and timing helpers."""
+
+    def __init__(self, fb, w, stream):
+        import torch
+
+        self.fb, self.w, self.s = fb, w, stream
+        self.x = make_input(w)
+        tdt = {"f32": torch.float32, "i16": torch.int16, "f16": torch.float16}
+        self.out_dtype = tdt[w.out_dtype]
+        self.plan = fb.fm_plan_create(w.sr, w.n_fft, w.hop, w.win_length, w.n_mels, w.f_min, w.f_max, w.power,
+                                      w.mel_scale, w.norm, w.in_dtype, w.out_dtype)
+        self.info = fb.fm_plan_get_info(self.plan)
+        self.nf = fb.fm_n_frames(self.plan, w.T)
+        xin = torch.from_numpy(self.x).cuda()
+        self.d_in = [xin.clone() for _ in range(BUFFER_SETS)]
+        self.d_out = [torch.empty((w.B, w.n_mels, self.nf), dtype=self.out_dtype, device="cuda")
+                      for _ in range(BUFFER_SETS)]
+        self.graphs = {}
+
+    def launch(self, i):
+        w = self.w
+        self.fb.fm_mel_forward(self.plan, self.d_in[i].data_ptr(), w.B, w.T, self.d_out[i].data_ptr(),
+                               self.s.cuda_stream)
+
+    def graph(self, n, same_set=False):
+        """A CUDA graph of n launches over sets 0..n-1 (or n launches on set 0)."""
+        import torch
+
+        key = (n, same_set)
+        if key not in self.graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.s):
+                for i in range(n):
+                    self.launch(0 if same_set else i)
+            with torch.cuda.stream(self.s):
+                g.replay()  # upload
+            self.s.synchronize()
+            self.graphs[key] = g
+        return self.graphs[key]
+
+    def warm(self, W):
+        import torch
+
+        with torch.cuda.stream(self.s):
+            for i in range(W):
+                self.launch(i % BUFFER_SETS)
+        self.s.synchronize()
+
+    def timed_steps_ms(self, K):
+        """Device time of exactly K launches replayed from graphs over the
+        rotating sets. A device-side wait queued ahead of the start event keeps
+        the host's graph submission out of the timed region."""
+        import torch
+
+        full, rest = divmod(K, BUFFER_SETS)
+        gs = [self.graph(BUFFER_SETS)] * full + ([self.graph(rest)] if rest else [])
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.s):
+            torch.cuda._sleep(HOST_SLACK_CYCLES)
+            a.record(self.s)
+            for g in gs:
+                g.replay()
+            z.record(self.s)
+        self.s.synchronize()
+        return a.elapsed_time(z)
+
+    def replay_us(self, g, n, reps):
+        import torch
+
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.s):
+            torch.cuda._sleep(HOST_SLACK_CYCLES)
+            a.record(self.s)
+            for _ in range(reps):
+                g.replay()
+            z.record(self.s)
+        self.s.synchronize()
+        return a.elapsed_time(z) * 1e3 / (n * reps)
+
+    def single_launch_us(self, n=32):
+        """Median device time of one launch on its own (nothing queued before or
+        after it, so no dependent-launch overlap: every launch pays its full
+        start-up and first-tile fetch)."""
+        import torch
+
+        ts = []
+        for i in range(n):
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(self.s):
+                torch.cuda._sleep(HOST_SLACK_CYCLES)
+                a.record(self.s)
+                self.launch(i % BUFFER_SETS)
+                z.record(self.s)
+            self.s.synchronize()
+            ts.append(a.elapsed_time(z) * 1e3)
+        return statistics.median(ts)
+
+    def figures(self, step_s, clk_mhz, props):
+        """Throughput, roofline and FP32 fractions for a step time."""
+        w = self.w
+        pk = peaks()
+        in_b, out_b = w.in_bytes(), w.out_bytes()
+        achieved = (in_b + out_b) / step_s / 1e9
+        flops = conventional_flops(w)
+        fp32_peak = props.multi_processor_count * 128 * 2 * clk_mhz * 1e6 / 1e12
+        return {
+            "frames_per_s": w.B * self.nf / step_s,
+            "audio_seconds_per_s": w.B * w.T / w.sr / step_s,
+            "hbm_gbs": achieved,
+            "roofline": {
+                "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"],
+                "peak_source": f"{pk['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": in_b + out_b,
+                "traffic": recorded_traffic(w.name),
+            },
+            "fp32": {"achieved_tflops": flops / step_s / 1e12, "peak_tflops": fp32_peak,
+                     "frac": flops / step_s / 1e12 / fp32_peak,
+                     "peak_basis": f"{props.multi_processor_count} SMs x 128 lanes x 2 x {clk_mhz:.0f} MHz",
+                     "ncu_fma_pipe_pct": recorded_fma_pipe(w.name)},
+        }
+
+    def close(self):
+        self.fb.fm_plan_destroy(self.plan)
+
+
 def run_gpu_arm(args) -> dict | None:
     import torch
     import torch.distributed as dist
@@ -176,93 +309,48 @@ def run_gpu_arm(args) -> dict | None:
     from mel_spectrogram_gb300 import _binding as fb
 
     w = WORKLOADS[args.workload]
-    x = make_input(w)
-    tdt = {"f32": torch.float32, "i16": torch.int16, "f16": torch.float16}
-    plan = fb.fm_plan_create(w.sr, w.n_fft, w.hop, w.win_length, w.n_mels, w.f_min, w.f_max, w.power,
-                             w.mel_scale, w.norm, w.in_dtype, w.out_dtype)
-    info = fb.fm_plan_get_info(plan)
-    nf = fb.fm_n_frames(plan, w.T)
-    xin = torch.from_numpy(x).cuda()
-    d_in = [xin.clone() for _ in range(BUFFER_SETS)]
-    d_out = [torch.empty((w.B, w.n_mels, nf), dtype=tdt[w.out_dtype], device="cuda") for _ in range(BUFFER_SETS)]
     s = torch.cuda.Stream()
-
-    def launch(i):
-        fb.fm_mel_forward(plan, d_in[i].data_ptr(), w.B, w.T, d_out[i].data_ptr(), s.cuda_stream)
-
+    run = WorkloadRun(fb, w, s)
     K, W = args.steps, args.warmup
-    with torch.cuda.stream(s):
-        for i in range(W):
-            launch(i % BUFFER_SETS)
-    s.synchronize()
-    graphs = {}
-    for n in sorted({BUFFER_SETS, K % BUFFER_SETS} - {0}):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for i in range(n):
-                launch(i)
-        graphs[n] = g
-    with torch.cuda.stream(s):  # upload and warm the graphs
-        for g in graphs.values():
-            g.replay()
-    s.synchronize()
+    run.warm(W)
+    run.graph(BUFFER_SETS)
+    if K % BUFFER_SETS:
+        run.graph(K % BUFFER_SETS)
 
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         t_start = time.time()
-        with torch.cuda.stream(s):
-            ev0.record(s)
-            for _ in range(K // BUFFER_SETS):
-                graphs[BUFFER_SETS].replay()
-            if K % BUFFER_SETS:
-                graphs[K % BUFFER_SETS].replay()
-            ev1.record(s)
-        s.synchronize()
+        ms = run.timed_steps_ms(K)
         torch.cuda.synchronize()
         t_end = time.time()
         if world > 1:
             dist.barrier()
-    ms = ev0.elapsed_time(ev1)
     if world > 1:
         t = torch.tensor([ms], device="cuda", dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     clocks = clk.summary(t_start, t_end)
-    assert fb.fm_plan_poll_error(plan) == fb.FM_OK
+    assert fb.fm_plan_poll_error(run.plan) == fb.FM_OK
 
-    # after the timed region: five repeats of the cold-L2 replay (median) and
-    # a warm-L2 replay that reuses one input/output set (labelled as such)
-    def replay_us(g, n, reps):
-        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(s):
-            a.record(s)
-            for _ in range(reps):
-                g.replay()
-            z.record(s)
-        s.synchronize()
-        return a.elapsed_time(z) * 1e3 / (n * reps)
-
+    # after the timed region: five repeats of the cold-L2 replay (median), a
+    # warm-L2 replay that reuses one input/output set, and single launches
+    # (all labelled, none of them the reported value)
     reps = max(1, min(K, 2000) // BUFFER_SETS)
-    repeat_us = [replay_us(graphs[BUFFER_SETS], BUFFER_SETS, reps) for _ in range(5)]
-    g_warm = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_warm, stream=s):
-        for _ in range(BUFFER_SETS):
-            launch(0)
-    replay_us(g_warm, BUFFER_SETS, 1)
-    warm_us = replay_us(g_warm, BUFFER_SETS, reps)
+    repeat_us = [run.replay_us(run.graph(BUFFER_SETS), BUFFER_SETS, reps) for _ in range(5)]
+    warm_us = run.replay_us(run.graph(BUFFER_SETS, same_set=True), BUFFER_SETS, reps)
+    single_us = run.single_launch_us()
 
     # end to end through the public C ABI with host buffers (copies in the region)
     Ke = max(3, min(K, args.e2e_steps))
-    h_in = torch.from_numpy(x).pin_memory()
-    h_out = torch.empty((w.B, w.n_mels, nf), dtype=tdt[w.out_dtype]).pin_memory()
+    h_in = torch.from_numpy(run.x).pin_memory()
+    h_out = torch.empty((w.B, w.n_mels, run.nf), dtype=run.out_dtype).pin_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def e2e_step(i):
-        fb.fm_mel_forward_host(plan, h_in.data_ptr(), w.B, w.T, h_out.data_ptr(), d_in[i].data_ptr(),
-                               d_out[i].data_ptr(), s.cuda_stream)
+        fb.fm_mel_forward_host(run.plan, h_in.data_ptr(), w.B, w.T, h_out.data_ptr(), run.d_in[i].data_ptr(),
+                               run.d_out[i].data_ptr(), s.cuda_stream)
 
     for i in range(3):
         e2e_step(i)
@@ -279,7 +367,40 @@ def run_gpu_arm(args) -> dict | None:
         t = torch.tensor([e_ms], device="cuda", dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e_ms = float(t.item())
-    fb.fm_plan_destroy(plan)
+    info, nf = run.info, run.nf
+    run.close()
+
+    # the other workloads, timed the same way on this rank (rank 0 reports them)
+    others = {}
+    if not args.only:
+        for name in ORDER:
+            if name == w.name:
+                continue
+            ow = WORKLOADS[name]
+            r2 = WorkloadRun(fb, ow, s)
+            K2 = min(K, args.other_steps)
+            r2.warm(W)
+            r2.graph(BUFFER_SETS)
+            if K2 % BUFFER_SETS:
+                r2.graph(K2 % BUFFER_SETS)
+            with ClockSampler(local) as c2:
+                torch.cuda.synchronize()
+                ta = time.time()
+                ms2 = r2.timed_steps_ms(K2)
+                torch.cuda.synchronize()
+                tb = time.time()
+            ck = c2.summary(ta, tb)
+            assert fb.fm_plan_poll_error(r2.plan) == fb.FM_OK
+            reps2 = max(1, min(K2, 2000) // BUFFER_SETS)
+            rep2 = statistics.median(r2.replay_us(r2.graph(BUFFER_SETS), BUFFER_SETS, reps2) for _ in range(3))
+            props = torch.cuda.get_device_properties(0)
+            fig = r2.figures(ms2 / 1e3 / K2, ck["sm_mhz"] or peaks()["sm_max_mhz"], props)
+            others[name] = {"metric": metric_for(ow), "workload": describe(ow), "steps": K2,
+                            "us_per_step": ms2 * 1e3 / K2, "repeats_median_us": rep2,
+                            "single_launch_us": r2.single_launch_us(16), **fig,
+                            "grid": min(r2.info["grid_limit"], ow.B * -(-r2.nf // r2.info["frames_per_tile"])),
+                            "block": r2.info["threads_per_block"], "clocks": ck}
+            r2.close()
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
@@ -289,13 +410,11 @@ def run_gpu_arm(args) -> dict | None:
     step_s = ms / 1e3 / K
     pk = peaks()
     in_b, out_b = w.in_bytes(), w.out_bytes()
-    achieved = (in_b + out_b) / step_s / 1e9
-    flops = conventional_flops(w)
     props = torch.cuda.get_device_properties(0)
     clk_mhz = clocks["sm_mhz"] or pk["sm_max_mhz"]
-    fp32_peak = props.multi_processor_count * 128 * 2 * clk_mhz * 1e6 / 1e12
+    fig = run.figures(step_s, clk_mhz, props)
     line = {
-        "metric": METRIC,
+        "metric": metric_for(w),
         "value": world * frames_step / step_s,
         "unit": "frames/s",
         "n_gpus": world,
@@ -313,27 +432,16 @@ def run_gpu_arm(args) -> dict | None:
             "in_dtype": w.in_dtype, "out_dtype": w.out_dtype,
             "l2": f"{BUFFER_SETS} rotating input/output sets, "
                   f"{BUFFER_SETS * (in_b + out_b) / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2",
-            "launch": f"CUDA graph of {BUFFER_SETS} fm_mel_forward launches, replayed",
+            "launch": f"CUDA graphs of {BUFFER_SETS} fm_mel_forward launches, replayed; a device-side wait "
+                      "queued ahead of the start event keeps host submission out of the timed region",
             "grid": min(info["grid_limit"], w.B * -(-nf // info["frames_per_tile"])),
             "block": info["threads_per_block"], "smem_bytes": info["smem_bytes"],
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
-        "audio_seconds_per_s": world * w.B * w.T / w.sr / step_s,
-        "hbm_gbs": achieved,
-        "roofline": {
-            "bound": "hbm",
-            "achieved": achieved,
-            "peak": pk["hbm_gbs"],
-            "unit": "GB/s",
-            "frac": achieved / pk["hbm_gbs"],
-            "peak_source": f"{pk['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-            "algorithmic_bytes_per_launch": in_b + out_b,
-            "traffic": recorded_traffic(w.name),
-        },
-        "fp32": {"achieved_tflops": flops / step_s / 1e12, "peak_tflops": fp32_peak,
-                 "frac": flops / step_s / 1e12 / fp32_peak,
-                 "peak_basis": f"{props.multi_processor_count} SMs x 128 lanes x 2 x {clk_mhz:.0f} MHz",
-                 "ncu_fma_pipe_pct": recorded_fma_pipe(w.name)},
+        "audio_seconds_per_s": world * fig["audio_seconds_per_s"],
+        "hbm_gbs": fig["hbm_gbs"],
+        "roofline": fig["roofline"],
+        "fp32": fig["fp32"],
         "e2e": {"value": world * frames_step * Ke / (e_ms / 1e3), "unit": "frames/s",
                 "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b, "steps": Ke,
                 "api": "fm_mel_forward_host (pinned host buffers; per step the upload, kernel and download "
@@ -343,11 +451,16 @@ def run_gpu_arm(args) -> dict | None:
                     "note": "cold L2 (16 rotating sets), timed after the main region"},
         "warm_l2": {"us_per_step": warm_us, "launches": reps * BUFFER_SETS,
                     "note": "one input/output set replayed: inputs and outputs stay in L2; not the reported value"},
+        "single_launch": {"us": single_us, "note": "one launch with nothing queued around it (no dependent-launch "
+                                                  "overlap with a previous call): the latency one isolated call "
+                                                  "sees; median of 32, not the reported value"},
         "gpu_launches": K,
         "clocks": clocks,
     }
+    if others:
+        line["workloads"] = others
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_baseline(w, x, args.cpu_seconds)
+        line["cpu_baseline"] = oracle_baseline(w, run.x, args.cpu_seconds)
     return line
 
 
@@ -413,7 +526,7 @@ def run_reference_arm(args) -> dict | None:
     v = fr * K / el
     sample = f"{fr} frames of signal 0 per step (first {seg.shape[1]} samples), {K} steps in {el:.1f} s"
     return {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": "frames/s", "n_gpus": world, "steps": K,
+        "impl": "reference", "metric": metric_for(w), "value": v, "unit": "frames/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": el * 1e3 / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": f"synthetic, seeded ({w.recipe}, seed {w.seed})",
         "config": {"workload": describe(w), "B": w.B, "T": w.T, "n_fft": w.n_fft, "hop": w.hop,
@@ -436,6 +549,9 @@ def main() -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", action="store_true", help="time the chosen workload only")
+    ap.add_argument("--other-steps", type=int, default=2000,
+                    help="timed steps of each of the other workloads (at most --steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
