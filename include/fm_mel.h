@@ -74,7 +74,8 @@ typedef enum { FM_NORMALIZED_NONE = 0, FM_NORMALIZED_WINDOW = 1, FM_NORMALIZED_F
  *   sr         : sample rate in Hz, > 0.
  *   n_fft      : DFT size. Supported: 400 and the powers of two 64 .. 16384
  *                (README "Usage": "400 or a power of 2 in [64, 16384]").
- *   hop        : frame advance in samples, > 0 and even.
+ *   hop        : frame advance in samples, > 0 (odd hops run a kernel that
+ *                stages each tile as one contiguous run of samples).
  *   win_length : Hann length, 1 .. n_fft; 0 means n_fft.
  *   n_mels     : number of mel filters, 1 .. 256.
  *   f_min      : lowest filter edge in Hz, >= 0.
@@ -96,7 +97,8 @@ typedef enum { FM_NORMALIZED_NONE = 0, FM_NORMALIZED_WINDOW = 1, FM_NORMALIZED_F
  *
  * Errors: FM_ERR_INVALID_ARG (out NULL or a parameter out of range, including
  * out_dtype == FM_I16); FM_ERR_UNSUPPORTED (n_fft not in the supported set,
- * n_mels > 256, odd hop); FM_ERR_CUDA (no usable device); FM_ERR_OOM.
+ * n_mels > 256, or a hop whose staged tile does not fit shared memory);
+ * FM_ERR_CUDA (no usable device); FM_ERR_OOM.
  */
 fm_status fm_plan_create(fm_plan** out, int sr, int n_fft, int hop, int win_length, int n_mels,
                          double f_min, double f_max, double power, fm_mel_scale mel_scale,

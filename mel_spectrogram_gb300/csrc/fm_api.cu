@@ -21,13 +21,23 @@
 namespace fm {
 extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant400h160, kVariant512,
     kVariant1024, kVariant2048, kVariant4096, kVariant8192, kVariant16384;
+extern const Variant kVariant64odd, kVariant128odd, kVariant256odd, kVariant400odd, kVariant512odd,
+    kVariant1024odd, kVariant2048odd;
 
+// The kernel for (n_fft, hop): a build for exactly this hop if there is one,
+// else the one for its parity (even hops stage and read aligned sample pairs,
+// odd hops take the generic kernel's contiguous staging), else one for any hop.
 const Variant* find_variant(int n_fft, int hop) {
-  static const Variant* all[] = {&kVariant400h160, &kVariant64,   &kVariant128,  &kVariant256,
-                                 &kVariant400,     &kVariant512,  &kVariant1024, &kVariant2048,
-                                 &kVariant4096,    &kVariant8192, &kVariant16384};
-  for (const Variant* v : all)
-    if (v->n_fft == n_fft && (v->hop == 0 || v->hop == hop)) return v;
+  static const Variant* all[] = {&kVariant400h160, &kVariant64,      &kVariant128,     &kVariant256,
+                                 &kVariant400,     &kVariant512,     &kVariant1024,    &kVariant2048,
+                                 &kVariant4096,    &kVariant8192,    &kVariant16384,   &kVariant64odd,
+                                 &kVariant128odd,  &kVariant256odd,  &kVariant400odd,  &kVariant512odd,
+                                 &kVariant1024odd, &kVariant2048odd};
+  const bool even = hop % 2 == 0;
+  for (const Variant* v : all) {
+    if (v->n_fft != n_fft) continue;
+    if (v->hop > 0 ? v->hop == hop : (v->hop == kAnyHop || (v->hop == kEvenHops) == even)) return v;
+  }
   return nullptr;
 }
 }  // namespace fm
@@ -273,7 +283,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   if (out_dtype != FM_F32 && out_dtype != FM_F16) return FM_ERR_INVALID_ARG;
   fm_status st = fm::check_filter_args(sr, n_fft, n_mels, f_min, &f_max, mel_scale, norm);
   if (st != FM_OK) return st;
-  if (!fm::is_supported_nfft(n_fft) || n_mels > 256 || (hop % 2) != 0) return FM_ERR_UNSUPPORTED;
+  if (!fm::is_supported_nfft(n_fft) || n_mels > 256) return FM_ERR_UNSUPPORTED;
   const fm::Variant* var = fm::find_variant(n_fft, hop);
   if (var == nullptr) return FM_ERR_UNSUPPORTED;
 

@@ -197,8 +197,13 @@ struct Variant {
   int in_buffers;       // 2: the next tile's input lands while this one computes
   int kind;             // 0: one frame per thread; 1: two frames per thread (packed); 2: shared-memory passes
   const void* fn;       // __global__ void(KernelParams)
-  int hop;              // > 0: compiled for this hop only; 0: any hop
+  int hop;              // > 0: compiled for this hop only; else kEvenHops, kOddHops or kAnyHop
 };
+
+// Variant::hop values other than a compiled-in hop
+constexpr int kEvenHops = 0;   // any even hop (samples staged and read in aligned pairs)
+constexpr int kOddHops = -1;   // any odd hop (contiguous staging, pairs read as two samples)
+constexpr int kAnyHop = -2;    // any hop (the large-transform kernel reads single samples)
 
 // the kernel for (n_fft, hop): a hop-specialised build if there is one
 const Variant* find_variant(int n_fft, int hop);

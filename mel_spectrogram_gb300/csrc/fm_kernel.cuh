@@ -165,6 +165,13 @@ __device__ __forceinline__ float2 load_pair(const __half* p) {
   return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
 
+// the same pair where it may start on an odd sample (odd hops): two scalar loads
+__device__ __forceinline__ float2 load_pair_odd(const float* p) { return make_float2(p[0], p[1]); }
+__device__ __forceinline__ float2 load_pair_odd(const short* p) { return make_float2((float)p[0], (float)p[1]); }
+__device__ __forceinline__ float2 load_pair_odd(const __half* p) {
+  return make_float2(__half2float(p[0]), __half2float(p[1]));
+}
+
 __device__ __forceinline__ float load_one(const float* p) { return __ldg(p); }
 __device__ __forceinline__ short load_one(const short* p) { return __ldg(p); }
 __device__ __forceinline__ __half load_one(const __half* p) { return __ldg(p); }
@@ -275,10 +282,44 @@ __device__ __forceinline__ void stage_tile(const Raw* __restrict__ src, long lon
   stage_rows_padded<Raw>(src, T, gstart, rows, hop, S, dst, warp, NWARPS, lane, ps);
 }
 
+// Staging for odd hops, where rows of one hop cannot keep sample pairs
+// aligned: the tile is one contiguous run of `len` samples from signal index
+// gstart (frame g starts at element g * hop). In-range samples arrive by
+// cp.async: f32 one per copy, 16-bit samples two per copy when the run starts
+// on a 4-byte boundary of the signal, else by plain loads. Padding goes
+// through padded_source; positions past the padded signal are left
+// untouched (no valid frame reads them). The caller commits, waits and
+// synchronises as for stage_tile.
+template <typename Raw>
+__device__ __noinline__ void stage_run(const Raw* __restrict__ src, long long T, long long gstart, int len, Raw* dst,
+                                       int tid, int nthreads, PadSpec ps) {
+  const long long end = T + ps.zpad + ps.cpad;  // one past the padded signal
+  if constexpr (sizeof(Raw) == 2) {
+    const bool pairs_ok = gstart >= 0 && gstart + len <= T && (reinterpret_cast<uintptr_t>(src + gstart) & 3) == 0;
+    if (pairs_ok) {
+      for (int i = 2 * tid; i + 1 < len; i += 2 * nthreads) cp_async<4>(dst + i, src + gstart + i);
+      if ((len & 1) && tid == 0) dst[len - 1] = load_one(src + gstart + len - 1);
+      return;
+    }
+  }
+  for (int i = tid; i < len; i += nthreads) {
+    const long long s = gstart + i;
+    if (s >= end) break;  // s only grows with i
+    const long long se = (s >= 0 && s < T) ? s : padded_source(s, T, ps);
+    if (se < 0) {
+      dst[i] = raw_zero<Raw>();
+    } else if constexpr (sizeof(Raw) == 4) {
+      cp_async<4>(dst + i, src + se);
+    } else {
+      dst[i] = load_one(src + se);
+    }
+  }
+}
+
 // Pass 1 for role p and frame g: windowed Q-point DFT of z[p + P q] and the
 // four-step twiddle W_M^{p k2}; writes row g of the exchange buffer at
 // [k2 * P + p].
-template <int P, int Q, typename Raw>
+template <int P, int Q, bool ODD, typename Raw>
 __device__ __forceinline__ void pass1(const Raw* __restrict__ frame_base, const float4* __restrict__ s_p1,
                                       const float2* __restrict__ s_twh, float2* xrow, int p) {
   float2 z[Q];
@@ -286,7 +327,8 @@ __device__ __forceinline__ void pass1(const Raw* __restrict__ frame_base, const 
 #pragma unroll
   for (int q = 0; q < Q; ++q) {
     const float4 e = tab[q];
-    const float2 v = load_pair(frame_base + __float_as_int(e.z));
+    const Raw* src = frame_base + __float_as_int(e.z);
+    const float2 v = ODD ? load_pair_odd(src) : load_pair(src);
     z[q] = make_float2(v.x * e.x, v.y * e.y);
   }
   dft<Q>(z);
@@ -473,7 +515,7 @@ __device__ __forceinline__ void mel_project(const float* s_pw, const int4* __res
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int N, int P, int Q, int G, int NBUF, typename Raw>
+template <int N, int P, int Q, int G, int NBUF, bool ODD, typename Raw>
 __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char* smem, const SmemLayout& lay) {
   constexpr int M = N / 2;
   constexpr int THREADS = P * G;
@@ -501,7 +543,10 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
     int tt;
     split(tile, b, tt);
     const long long t0 = (long long)tt * G;
-    stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.lead, rows, hop, S, in_buf(buf), warp, lane, pads);
+    if constexpr (ODD)  // rows of one odd hop, back to back (S == hop)
+      stage_run<Raw>(in + b * T, T, t0 * hop - prm.lead, rows * hop, in_buf(buf), tid, THREADS, pads);
+    else
+      stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.lead, rows, hop, S, in_buf(buf), warp, lane, pads);
     cp_async_commit();
   };
 
@@ -515,7 +560,7 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
     if (NBUF == 2 && next < prm.total_tiles) stage(next, buf ^ 1);
 
     float2* xrow = s_x + g * GS;
-    pass1<P, Q, Raw>(in_buf(buf) + g * S, s_p1, s_twh, xrow, role);
+    pass1<P, Q, ODD, Raw>(in_buf(buf) + g * S, s_p1, s_twh, xrow, role);
     __syncthreads();
     if (NBUF == 1 && next < prm.total_tiles) stage(next, 0);  // pass 1 was the last reader
 
@@ -547,7 +592,7 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
   cp_async_wait_all();
 }
 
-template <int N, int P, int Q, int G, int NBUF>
+template <int N, int P, int Q, int G, int NBUF, bool ODD>
 __global__ void __launch_bounds__(P* G) mel_kernel(const KernelParams prm) {
   constexpr int M = N / 2;
   constexpr int THREADS = P * G;
@@ -570,16 +615,20 @@ __global__ void __launch_bounds__(P* G) mel_kernel(const KernelParams prm) {
   pdl_wait();  // caller buffers only after the previous kernel in the stream is done
   // (the first barrier inside run_tiles publishes the tables)
 
-  if (prm.in_dtype == FM_F32) run_tiles<N, P, Q, G, NBUF, float>(prm, smem, lay);
-  else if (prm.in_dtype == FM_I16) run_tiles<N, P, Q, G, NBUF, short>(prm, smem, lay);
-  else run_tiles<N, P, Q, G, NBUF, __half>(prm, smem, lay);
+  if (prm.in_dtype == FM_F32) run_tiles<N, P, Q, G, NBUF, ODD, float>(prm, smem, lay);
+  else if (prm.in_dtype == FM_I16) run_tiles<N, P, Q, G, NBUF, ODD, short>(prm, smem, lay);
+  else run_tiles<N, P, Q, G, NBUF, ODD, __half>(prm, smem, lay);
 }
 
 }  // namespace fm
 
-// Instantiate one variant: FM_DEFINE_VARIANT(name, N, P, Q, G, NBUF)
-#define FM_DEFINE_VARIANT(NAME, N, P, Q, G, NBUF)                                                       \
+// Instantiate one variant: FM_DEFINE_VARIANT(name, N, P, Q, G, NBUF) for even
+// hops, FM_DEFINE_VARIANT_ODD(...) for odd ones
+#define FM_DEFINE_VARIANT_HOPS(NAME, N, P, Q, G, NBUF, ODD, HOPS)                                      \
   namespace fm {                                                                                        \
-  template __global__ void mel_kernel<N, P, Q, G, NBUF>(const KernelParams);                          \
-  extern const Variant NAME = {N, P, Q, G, P * G, NBUF, 0, (const void*)&mel_kernel<N, P, Q, G, NBUF>, 0}; \
+  template __global__ void mel_kernel<N, P, Q, G, NBUF, ODD>(const KernelParams);                     \
+  extern const Variant NAME = {N,    P, Q, G, P * G, NBUF, 0, (const void*)&mel_kernel<N, P, Q, G, NBUF, ODD>, \
+                               HOPS};                                                                   \
   }
+#define FM_DEFINE_VARIANT(NAME, N, P, Q, G, NBUF) FM_DEFINE_VARIANT_HOPS(NAME, N, P, Q, G, NBUF, false, kEvenHops)
+#define FM_DEFINE_VARIANT_ODD(NAME, N, P, Q, G, NBUF) FM_DEFINE_VARIANT_HOPS(NAME, N, P, Q, G, NBUF, true, kOddHops)

@@ -217,5 +217,5 @@ __global__ void __launch_bounds__(kBigThreads, 1) mel_kernel_big(const KernelPar
   namespace fm {                                                                                     \
   template __global__ void mel_kernel_big<N>(const KernelParams);                                   \
   extern const Variant NAME = {N, 0, 0, big_frames(N), kBigThreads, 0, 2,                            \
-                               (const void*)&mel_kernel_big<N>, 0};                                  \
+                               (const void*)&mel_kernel_big<N>, kAnyHop};                            \
   }

@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(kX2Groups* P* kX2Lanes + 32 * kX2ProducerWarps
 }  // namespace fm
 
 // Instantiate one two-frames-per-thread variant:
-// FM_DEFINE_VARIANT_X2(name, N, P, Q, HOP) with HOP = 0 for any hop
+// FM_DEFINE_VARIANT_X2(name, N, P, Q, HOP) with HOP = 0 for any even hop
 #define FM_DEFINE_VARIANT_X2(NAME, N, P, Q, HOP)                                                       \
   namespace fm {                                                                                       \
   template __global__ void mel_kernel_x2<N, P, Q, HOP>(const __grid_constant__ KernelParams);        \
