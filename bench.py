@@ -27,7 +27,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from mel_spectrogram_gb300.workloads import ORDER, WORKLOADS, make_input  # noqa: E402
+from mel_spectrogram_gb300.workloads import EXTRA, ORDER, WORKLOADS, make_input  # noqa: E402
 
 BUFFER_SETS = 16
 HOST_SLACK_CYCLES = 200_000  # ~0.1 ms of device-side wait ahead of a timed region
@@ -373,7 +373,7 @@ def run_gpu_arm(args) -> dict | None:
     # the other workloads, timed the same way on this rank (rank 0 reports them)
     others = {}
     if not args.only:
-        for name in ORDER:
+        for name in ORDER + EXTRA:
             if name == w.name:
                 continue
             ow = WORKLOADS[name]

@@ -143,14 +143,19 @@ typedef struct {
 fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* params);
 
 /* fm_plan_destroy -- free the plan's device tables. NULL is accepted (no-op).
+ * The pages have no counterpart (flashmel keeps its per-configuration
+ * modules and filter buffers in process-wide caches, README "How it works");
+ * here the plan owns them and this call releases them.
  * Work already queued with the plan must have finished (e.g. synchronise the
  * streams first). Returns FM_OK, or FM_ERR_CUDA if freeing failed. */
 fm_status fm_plan_destroy(fm_plan* plan);
 
 /* fm_n_frames -- frames per signal for T samples: with T' = T + 2 * pad,
- * 1 + floor(T' / hop) when centred, 1 + floor((T' - n_fft) / hop) when not
- * (torch.stft). Returns -1 if plan is NULL or T is too short for the plan's
- * framing (see fm_mel_forward). */
+ * 1 + floor(T' / hop) when centred, 1 + floor((T' - n_fft) / hop) when not.
+ * flashmel README "Usage": the output is (..., n_mels, n_frames) like
+ * torchaudio's, e.g. 480000 samples at hop 160, centred, give 3001 frames.
+ * Returns -1 if plan is NULL or T is too short for the plan's framing (see
+ * fm_mel_forward). */
 int64_t fm_n_frames(const fm_plan* plan, int64_t T);
 
 /*
@@ -233,6 +238,9 @@ fm_status fm_mel_forward_host(const fm_plan* plan, const void* h_in, int64_t B, 
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, which may make the CUDA runtime load this library's
  * module on that device); make that first call before any stream capture.
+ * The address is looked up again when the current context of the device is
+ * not the one it was looked up in (after cudaDeviceReset, or under a context
+ * the caller made current), so that call too belongs outside a capture.
  * The caller synchronises `stream` before reading h_out; pinned host memory
  * makes the copies asynchronous.
  * Errors: as fm_mel_forward_host, plus FM_ERR_INVALID_ARG for sizes beyond
@@ -306,17 +314,28 @@ typedef struct {
 fm_status fm_plan_get_info(const fm_plan* plan, fm_plan_info* info);
 
 /*
- * fm_plan_poll_error -- read and clear the plan's device error word
- * (synchronising the plan's device). Kernels that wait on a device-side
+ * fm_plan_poll_error -- read and clear the plan's device error word. The
+ * pages have no counterpart (flashmel's kernels wait on nothing that can be
+ * lost); this is the report channel of the bounded waits below.
+ * Kernels that wait on a device-side
  * barrier give up after a bounded number of polls, about a second on GB300
  * (a tile group's wait for its staged tile: 2^18 mbarrier.try_wait polls of
  * about 3.8 us; the producer warp's wait for a free staging area: 2^22
  * test_wait polls of about 0.1 us). They then record FM_ERR_KERNEL_TIMEOUT
- * there and return instead of hanging. Returns FM_OK if nothing was recorded.
+ * there and return instead of hanging. The word is read and cleared in one
+ * atomic exchange on the device (a one-thread kernel on the legacy default
+ * stream), then copied back, so a code that a kernel still running records
+ * in between is kept for the next poll rather than lost. The result covers
+ * the kernels that have finished: call it after synchronising every stream
+ * that used the plan to see all of them. Returns FM_OK if nothing was
+ * recorded, FM_ERR_CUDA if the exchange or the copy failed.
  */
 fm_status fm_plan_poll_error(const fm_plan* plan);
 
-/* fm_status_string -- a static, human-readable name for a status code. */
+/* fm_status_string -- a static, human-readable name for a status code
+ * ("FM_OK", "FM_ERR_INVALID_ARG", ...; "FM_ERR_UNKNOWN" for any other value).
+ * The pages have no counterpart: flashmel raises Python exceptions, and
+ * errors cross this C ABI as status codes instead. */
 const char* fm_status_string(fm_status status);
 
 #ifdef __cplusplus

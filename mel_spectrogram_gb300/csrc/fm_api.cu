@@ -76,6 +76,7 @@ struct fm_plan {
   fm::X2Tables* x2;  // device tables of the two-frames-per-thread kernel (inside dmem)
   mutable HostPipe pipe;  // streams and events of fm_mel_forward_host
   int x2_slots;         // its mel chunk slots
+  int big_span;         // large-transform kernel: samples staged per tile (0: loads from global memory)
 };
 
 namespace {
@@ -313,7 +314,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   if (cudaGetDevice(&dev) != cudaSuccess) return FM_ERR_CUDA;
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
   const int in_esize = in_dtype == FM_F32 ? 4 : 2;
-  const size_t smem_total =
+  size_t smem_total =
       var->kind == 1   ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize, fm::kX2Groups).total
       : var->kind == 2 ? fm::big_smem_bytes(n_fft)
                        : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
@@ -327,6 +328,16 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
                              ? prop.sharedMemPerBlockOptin - fattr.sharedSizeBytes
                              : 0;
   if (smem_total > dyn_max) return FM_ERR_UNSUPPORTED;
+  // large-transform kernel: a staging buffer for the next tile's samples, when
+  // one tile's span fits beside the transform buffer
+  int big_span = 0;
+  if (var->kind == 2) {
+    const size_t st_bytes = fm::big_staging_bytes(n_fft, hop, in_esize);
+    if (fm::big_span(n_fft, hop) < (1 << 24) && smem_total + st_bytes <= dyn_max) {
+      big_span = (int)fm::big_span(n_fft, hop);
+      smem_total += st_bytes;
+    }
+  }
   // allow the device maximum once, so plans of different sizes never undercut each other
   if (cudaFuncSetAttribute(var->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_max) != cudaSuccess)
     return FM_ERR_CUDA;
@@ -359,6 +370,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   p->var = var;
   p->nnz = nnz;
   p->x2_slots = x2_slots;
+  p->big_span = big_span;
   p->smem = smem_total;
   p->blocks_per_sm = bps;
   p->num_sms = prop.multiProcessorCount;
@@ -516,6 +528,7 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.mel_w = plan->mel_w;
   prm.err = plan->err;
   prm.win = plan->win;
+  prm.big_span = plan->big_span;
 
   const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
   prm.x2 = plan->x2;
@@ -649,13 +662,19 @@ extern "C" fm_status fm_plan_get_info(const fm_plan* plan, fm_plan_info* info) {
 
 unsigned* fm::plan_error_word(const fm_plan* plan) { return plan ? plan->err : nullptr; }
 
+// err[0] is the error word the kernels write; err[1] receives its value when
+// fm_plan_poll_error takes and clears it in one atomic exchange.
+__global__ void take_error_word(unsigned* err) { err[1] = atomicExch(err, 0u); }
+
 extern "C" fm_status fm_plan_poll_error(const fm_plan* plan) {
   if (plan == nullptr) return FM_ERR_INVALID_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device) return FM_ERR_CUDA;
+  take_error_word<<<1, 1>>>(plan->err);
+  if (cudaGetLastError() != cudaSuccess) return FM_ERR_CUDA;
   unsigned word = 0;
-  if (cudaMemcpy(&word, plan->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FM_ERR_CUDA;
+  if (cudaMemcpy(&word, plan->err + 1, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FM_ERR_CUDA;
   if (word == 0) return FM_OK;
-  const unsigned zero = 0;
-  if (cudaMemcpy(plan->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FM_ERR_CUDA;
   return word <= FM_ERR_KERNEL_TIMEOUT ? (fm_status)word : FM_ERR_KERNEL_TIMEOUT;
 }
 

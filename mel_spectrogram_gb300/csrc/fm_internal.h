@@ -47,6 +47,7 @@ struct KernelParams {
   int x2_slots;               // its mel chunk slots (X2Tables::desc rows in use)
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
   const float* win;       // the n_fft-point window (large-transform kernel only)
+  int big_span;           // large-transform kernel: samples staged per tile in shared memory (0: none)
   // Packed kernel: when tmap_ok, every signal is described to the TMA unit as
   // rows of one staged line (line * in_bytes / 8 elements of 8 bytes) that
   // start at sample tmap_off + y * line, tmap_rows rows per signal, and the

@@ -54,6 +54,15 @@ __host__ __device__ constexpr int big_frame_stride(int M) { return M + (M >> 4) 
 __host__ __device__ constexpr size_t big_smem_bytes(int n_fft) {
   return sizeof(float2) * (size_t)big_frames(n_fft) * (size_t)big_frame_stride(n_fft / 2);
 }
+// Samples one tile's frames cover, (F - 1) hop + n_fft: the span the kernel
+// prefetches into a staging buffer behind the transform buffer when it fits
+// (KernelParams::big_span), 16-byte aligned.
+__host__ __device__ constexpr long long big_span(int n_fft, int hop) {
+  return (long long)(big_frames(n_fft) - 1) * hop + n_fft;
+}
+__host__ __device__ constexpr size_t big_staging_bytes(int n_fft, int hop, int esize) {
+  return (size_t)((big_span(n_fft, hop) * esize + 15) / 16 * 16);
+}
 __device__ __forceinline__ int big_phys(int i) { return i + (i >> 4); }
 
 __device__ __forceinline__ float raw_to_float(float v) { return v; }
@@ -71,23 +80,48 @@ __device__ __forceinline__ float big_sample(const Raw* __restrict__ sig, long lo
 // Windowed pairs of F frames: frame f starts at signal index s0 + f hop;
 // z[n] = (y[2n], y[2n+1]) times (w[2n], w[2n+1]) (the window carries the 1/2 of
 // the split, the STFT normalisation and the int16 scale).
+// Every global load of the tile is issued before the first one is used (the
+// loop has a compile-time trip count), so the tile waits for one memory
+// latency rather than one per few pairs.
 template <int N, typename Raw>
 __device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ sig, long long T, long long s0,
                                          int hop, const float2* __restrict__ win2, const PadSpec& ps, int tid) {
   constexpr int M = N / 2, F = big_frames(N), FS = big_frame_stride(M);
-  for (int idx = tid; idx < F * M; idx += kBigThreads) {
-    const int f = idx / M, n = idx % M;
+  constexpr int PER = F * M / kBigThreads;
+  static_assert((F * M) % kBigThreads == 0, "pairs must divide evenly over the threads");
+  const bool interior = s0 >= 0 && s0 + (long long)(F - 1) * hop + N <= T;
+  float2 v[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
     const long long s = s0 + (long long)f * hop + 2 * n;
-    float a, b;
-    if (s >= 0 && s + 1 < T) {
-      a = raw_to_float(sig[s]);
-      b = raw_to_float(sig[s + 1]);
+    if (interior) {
+      v[i] = make_float2(raw_to_float(sig[s]), raw_to_float(sig[s + 1]));
     } else {
-      a = big_sample(sig, T, s, ps);
-      b = big_sample(sig, T, s + 1, ps);
+      v[i] = make_float2(big_sample(sig, T, s, ps), big_sample(sig, T, s + 1, ps));
     }
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
     const float2 w = __ldg(win2 + n);
-    s_x[f * FS + big_phys(n)] = make_float2(a * w.x, b * w.y);
+    s_x[f * FS + big_phys(n)] = make_float2(v[i].x * w.x, v[i].y * w.y);
+  }
+}
+
+// The same from a staging buffer that holds the tile's padded samples
+// (st[i] = the sample at padded position s0 + i, see stage_run).
+template <int N, typename Raw>
+__device__ __forceinline__ void big_load_staged(float2* s_x, const Raw* st, int hop, const float2* __restrict__ win2,
+                                                int tid) {
+  constexpr int M = N / 2, F = big_frames(N), FS = big_frame_stride(M);
+  constexpr int PER = F * M / kBigThreads;
+#pragma unroll 8
+  for (int i = 0; i < PER; ++i) {
+    const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
+    const Raw* p = st + f * hop + 2 * n;
+    const float2 w = __ldg(win2 + n);
+    s_x[f * FS + big_phys(n)] = make_float2(raw_to_float(p[0]) * w.x, raw_to_float(p[1]) * w.y);
   }
 }
 
@@ -173,14 +207,31 @@ __device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned 
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
   const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
+  // With a staging buffer (prm.big_span > 0), the next tile's samples are
+  // prefetched by cp.async while this tile's transform runs.
+  Raw* s_st = reinterpret_cast<Raw*>(smem + big_smem_bytes(N));
+  const int span = prm.big_span;
+  auto prefetch = [&](long long t) {
+    long long bb;
+    int tq;
+    split(t, bb, tq);
+    stage_run<Raw>(in + bb * T, T, (long long)tq * F * prm.hop - prm.lead, span, s_st, tid, kBigThreads, pads);
+    cp_async_commit();
+  };
+  if (span > 0 && (long long)blockIdx.x < prm.total_tiles) prefetch(blockIdx.x);
   for (long long tile = blockIdx.x; tile < prm.total_tiles; tile += gridDim.x) {
     long long b;
     int tt;
     split(tile, b, tt);
     const int t0 = tt * F;
-    __syncthreads();  // the previous tile's mel reads are done
-    big_load<N, Raw>(s_x, in + b * T, T, (long long)t0 * prm.hop - prm.lead, prm.hop, win2, pads, tid);
+    if (span > 0) cp_async_wait_all();  // this thread's copies of the tile have landed
+    __syncthreads();  // the previous tile's mel reads are done; the staged tile is visible
+    if (span > 0)
+      big_load_staged<N, Raw>(s_x, s_st, prm.hop, win2, tid);
+    else
+      big_load<N, Raw>(s_x, in + b * T, T, (long long)t0 * prm.hop - prm.lead, prm.hop, win2, pads, tid);
     __syncthreads();
+    if (span > 0 && tile + gridDim.x < prm.total_tiles) prefetch(tile + gridDim.x);  // staging read: reuse it
     big_pass<M, F, R0, 1>(s_x, prm.tw_half, tid);
     big_pass<M, F, R1, R0>(s_x, prm.tw_half, tid);
     big_pass<M, F, R2, R0 * R1>(s_x, prm.tw_half, tid);
@@ -198,6 +249,7 @@ __device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned 
       mel_project<F, NWARPS, M + 1>(s_pw, prm.mel, prm.mel_w, static_cast<__half*>(prm.out) + obase, n_valid,
                                     prm.n_mels, prm.n_frames, warp, lane);
   }
+  cp_async_wait_all();  // nothing stays in flight past the end of the CTA
 }
 
 template <int N>

@@ -9,7 +9,9 @@
 // them; this entry point needs none. It stages the input and the output in
 // one array of FM_NOALLOC_MAX_BYTES that every GPU loading this library holds
 // until the process exits, and calls no allocating routine.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -28,17 +30,45 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_staging[kStagingBytes];
 
 std::mutex g_setup_mu;
-unsigned char* g_staging_addr[kMaxDevices];  // device address of g_staging, per device
+// device address of g_staging per device, and the context it was looked up in
+unsigned char* g_staging_addr[kMaxDevices];
+CUcontext g_staging_ctx[kMaxDevices];
 
-// The array's device address on `dev` (the current device), looked up once.
-// In host code g_staging names a host-side shadow, never device memory.
+// cuCtxGetCurrent from the driver, resolved once through the runtime (no link
+// against libcuda); null if unavailable.
+PFN_cuCtxGetCurrent_v4000 ctx_getter() {
+  static const PFN_cuCtxGetCurrent_v4000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (PFN_cuCtxGetCurrent_v4000) nullptr;
+    return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  }();
+  return fn;
+}
+
+// The array's device address on `dev` (the current device). It is looked up
+// the first time a context of `dev` is current here, and again whenever the
+// current context differs from the one it was looked up in (a context
+// created by the caller, or the primary context after cudaDeviceReset), so a
+// stale address is never used. In host code g_staging names a host-side
+// shadow, never device memory.
 fm_status staging_address(int dev, unsigned char** out) {
   if (dev < 0 || dev >= kMaxDevices) return FM_ERR_UNSUPPORTED;
+  const PFN_cuCtxGetCurrent_v4000 get_ctx = ctx_getter();
+  if (get_ctx == nullptr) return FM_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return FM_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (g_staging_addr[dev] == nullptr) {
+  // no context bound to this thread yet (ctx null): the look-up binds the
+  // device's primary context, which is then read back
+  if (ctx == nullptr || g_staging_addr[dev] == nullptr || g_staging_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_staging) != cudaSuccess || p == nullptr) return FM_ERR_CUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return FM_ERR_CUDA;
     g_staging_addr[dev] = static_cast<unsigned char*>(p);
+    g_staging_ctx[dev] = ctx;
   }
   *out = g_staging_addr[dev];
   return FM_OK;

@@ -10,7 +10,7 @@ import pytest
 
 from mel_spectrogram_gb300 import _binding as fb
 from mel_spectrogram_gb300.workloads import WORKLOADS, Workload, make_input
-from tests.gpu_util import check_close, oracle_for, plan_for, run_gpu, torch_dtype
+from tests.gpu_util import check_close, check_close_saturating, oracle_for, plan_for, run_gpu, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -365,3 +365,23 @@ def test_plan_info():
         assert info["nnz"] > 0
     finally:
         fb.fm_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(n_fft=400, hop=160, n_mels=128, T=16000, scale=12.0),  # two-frame kernel
+    dict(n_fft=1024, hop=256, n_mels=80, T=20000, scale=8.0),
+    dict(n_fft=2048, hop=512, n_mels=128, T=30000, scale=300.0, power=1.0, in_dtype="f16"),
+    dict(n_fft=8192, hop=2048, n_mels=128, T=40000, scale=0.7),  # shared-memory passes
+], ids=lambda k: f"n{k['n_fft']}")
+def test_f16_output_saturates_to_inf(kw):
+    """Loud signals whose mel values straddle the f16 range: +inf exactly where
+    the float64 oracle overflows f16, the f16 tolerance elsewhere."""
+    kw = dict(kw)
+    scale = kw.pop("scale")
+    in_dtype = kw.pop("in_dtype", "f32")
+    w = W(out_dtype="f16", in_dtype=in_dtype, win_length=kw["n_fft"], **kw)
+    x = (make_input(dataclasses.replace(w, in_dtype="f32", recipe="normal")).astype(np.float64) * scale)
+    x = x.astype(np.float16 if in_dtype == "f16" else np.float32)
+    ref = oracle_for(w, x)
+    n_inf, n_fin = check_close_saturating(run_gpu(w, x), ref, str(kw))
+    assert n_inf > 0 and n_fin > 0, (n_inf, n_fin)  # the case really straddles the range
