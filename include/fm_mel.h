@@ -46,7 +46,9 @@ typedef enum {
   FM_ERR_UNSUPPORTED = 2,    /* valid for torchaudio, but not built here (see fm_plan_create) */
   FM_ERR_CUDA = 3,           /* a CUDA runtime call failed (no device, launch failure, ...) */
   FM_ERR_OOM = 4,            /* device or host allocation failed */
-  FM_ERR_KERNEL_TIMEOUT = 5  /* a bounded device-side wait gave up (reported by fm_plan_poll_error) */
+  FM_ERR_KERNEL_TIMEOUT = 5, /* a bounded device-side wait gave up (reported by fm_plan_poll_error) */
+  FM_ERR_BOUNDS = 6          /* debug build only (libfm_mel_check.so, -DFM_BOUNDS_CHECK): an index check
+                                found an access outside its buffer and skipped it (fm_plan_poll_error) */
 } fm_status;
 
 typedef enum { FM_MEL_HTK = 0, FM_MEL_SLANEY = 1 } fm_mel_scale;

@@ -6,13 +6,17 @@ library has not been built this module raises; there is no fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfm_mel.so")
+# the debug build: the same kernels with an index check on every guarded
+# access (-DFM_BOUNDS_CHECK), built beside the release library
+CHECK_LIB_PATH = os.path.join(_HERE, "libfm_mel_check.so")
 
-FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_CUDA, FM_ERR_OOM, FM_ERR_KERNEL_TIMEOUT = range(6)
+FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_CUDA, FM_ERR_OOM, FM_ERR_KERNEL_TIMEOUT, FM_ERR_BOUNDS = range(7)
 FM_MEL_HTK, FM_MEL_SLANEY = 0, 1
 FM_NORM_NONE, FM_NORM_SLANEY = 0, 1
 FM_F32, FM_I16, FM_F16 = 0, 1, 2
@@ -62,19 +66,41 @@ class fm_plan_params(C.Structure):
 
 
 _lib = None
+_loaded: dict[str, C.CDLL] = {}
 
 
 def lib() -> C.CDLL:
     """Load libfm_mel.so (built by mel_spectrogram_gb300.build); raise if absent."""
     global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
+    if _lib is None:
+        _lib = load(LIB_PATH)
+    return _lib
+
+
+@contextlib.contextmanager
+def library(path: str):
+    """Route every call of this module through the library at `path` (e.g.
+    CHECK_LIB_PATH, the debug build) inside the block. Plans are bound to
+    the library that created them: create and destroy them inside one block."""
+    global _lib
+    prev = _lib
+    _lib = load(path)
+    try:
+        yield _lib
+    finally:
+        _lib = prev
+
+
+def load(path: str) -> C.CDLL:
+    """Load one build of the library with its prototypes declared (cached)."""
+    if path in _loaded:
+        return _loaded[path]
+    if not os.path.exists(path):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it with `python -m mel_spectrogram_gb300.build` "
+            f"{path} is missing: build it with `python -m mel_spectrogram_gb300.build` "
             "(the mel path has no CPU fallback)"
         )
-    L = C.CDLL(LIB_PATH)
+    L = C.CDLL(path)
     vp, i64, ci, cd = C.c_void_p, C.c_int64, C.c_int, C.c_double
     L.fm_plan_create.argtypes = [C.POINTER(vp), ci, ci, ci, ci, ci, cd, cd, cd, ci, ci, ci, ci]
     L.fm_plan_create.restype = ci
@@ -100,7 +126,7 @@ def lib() -> C.CDLL:
     L.fm_status_string.restype = C.c_char_p
     L.fm_selftest_wait_timeout.argtypes = [vp, ci, ci, vp, C.POINTER(ci), C.POINTER(cd)]
     L.fm_selftest_wait_timeout.restype = ci
-    _lib = L
+    _loaded[path] = L
     return L
 
 

@@ -316,7 +316,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   const int in_esize = in_dtype == FM_F32 ? 4 : 2;
   size_t smem_total =
       var->kind == 1   ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize, fm::kX2Groups).total
-      : var->kind == 2 ? fm::big_smem_bytes(n_fft)
+      : var->kind == 2 ? fm::big_layout(n_fft, n_mels, nnz).st
                        : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
   if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_slots > fm::kX2MaxSlots ||
                          x2_warps > fm::kX2MaxWarps))
@@ -675,7 +675,7 @@ extern "C" fm_status fm_plan_poll_error(const fm_plan* plan) {
   unsigned word = 0;
   if (cudaMemcpy(&word, plan->err + 1, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FM_ERR_CUDA;
   if (word == 0) return FM_OK;
-  return word <= FM_ERR_KERNEL_TIMEOUT ? (fm_status)word : FM_ERR_KERNEL_TIMEOUT;
+  return word <= FM_ERR_BOUNDS ? (fm_status)word : FM_ERR_KERNEL_TIMEOUT;
 }
 
 extern "C" const char* fm_status_string(fm_status status) {
@@ -686,6 +686,7 @@ extern "C" const char* fm_status_string(fm_status status) {
     case FM_ERR_CUDA: return "FM_ERR_CUDA";
     case FM_ERR_OOM: return "FM_ERR_OOM";
     case FM_ERR_KERNEL_TIMEOUT: return "FM_ERR_KERNEL_TIMEOUT";
+    case FM_ERR_BOUNDS: return "FM_ERR_BOUNDS";
   }
   return "FM_ERR_UNKNOWN";
 }

@@ -9,6 +9,22 @@
 
 namespace fm {
 
+// Index checks of the debug build (compiled with -DFM_BOUNDS_CHECK into
+// libfm_mel_check.so). A guarded access is written `if (FM_IN(ok, err)) ...`
+// with `ok` its index test against the buffer it touches: on a miss the
+// kernel records FM_ERR_BOUNDS in the plan's error word (err) and skips the
+// access, so a wrong index shows up as a status, never as a fault or a trap.
+// In the normal build FM_IN is `true` and the tests compile away.
+#ifdef FM_BOUNDS_CHECK
+__device__ __forceinline__ bool fm_in_bounds(bool ok, unsigned* err) {
+  if (!ok && err != nullptr) atomicExch(err, (unsigned)FM_ERR_BOUNDS);
+  return ok;
+}
+#define FM_IN(ok, err) ::fm::fm_in_bounds((ok), (err))
+#else
+#define FM_IN(ok, err) true
+#endif
+
 // Everything one launch needs. Passed by value (it lives in the kernel's
 // parameter constant bank), so the kernel reads it without global loads.
 struct KernelParams {

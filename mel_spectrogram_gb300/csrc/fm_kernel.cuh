@@ -208,6 +208,26 @@ __device__ __forceinline__ long long padded_source(long long s, long long T, con
   return (src >= 0 && src < T) ? src : -1;
 }
 
+// The length in elements of the buffer a guarded access touches, and the
+// plan's error word: what the debug build's index checks (FM_IN) compare
+// against. The normal build never reads it.
+struct Cap {
+  int n;
+  unsigned* err;
+};
+
+// Element i of a row that starts at element `off` of a buffer of cap.n
+// elements: stored / loaded only if it lies inside the buffer (checked in the
+// debug build; a plain access otherwise).
+template <typename T>
+__device__ __forceinline__ void put(T* row, int off, int i, const T& v, Cap cap) {
+  if (FM_IN(off + i >= 0 && off + i < cap.n, cap.err)) row[i] = v;
+}
+template <typename T>
+__device__ __forceinline__ T get(const T* row, int off, int i, Cap cap) {
+  return FM_IN(off + i >= 0 && off + i < cap.n, cap.err) ? row[i] : T{};
+}
+
 // The general staging path of stage_tile: rows [0, rows) of hop samples from
 // signal index gstart, in-range aligned pairs as one cp.async, every other
 // sample through padded_source. Positions from the end of the padded signal
@@ -217,7 +237,7 @@ __device__ __forceinline__ long long padded_source(long long s, long long T, con
 template <typename Raw>
 __device__ __noinline__ void stage_rows_padded(const Raw* __restrict__ src, long long T, long long gstart, int rows,
                                                int hop, int S, Raw* dst, int warp, int nwarps, int lane,
-                                               PadSpec ps) {
+                                               PadSpec ps, Cap cap) {
   const bool aligned = ((reinterpret_cast<uintptr_t>(src + gstart)) % (2 * sizeof(Raw))) == 0;
   const int pairs = hop / 2;
   const long long end = T + ps.zpad + ps.cpad;  // one past the padded signal
@@ -232,7 +252,7 @@ __device__ __noinline__ void stage_rows_padded(const Raw* __restrict__ src, long
     for (int c2 = lane; c2 < c2_end; c2 += 32) {
       const long long s = s0 + 2 * c2;
       if (aligned && s >= 0 && s + 1 < T) {
-        cp_async<2 * sizeof(Raw)>(d + 2 * c2, src + s);
+        if (FM_IN(r * S + 2 * c2 + 1 < cap.n, cap.err)) cp_async<2 * sizeof(Raw)>(d + 2 * c2, src + s);
         continue;
       }
 #pragma unroll
@@ -246,6 +266,7 @@ __device__ __noinline__ void stage_rows_padded(const Raw* __restrict__ src, long
           se = padded_source(se, T, ps);
         }
         Raw* de = d + 2 * c2 + e;
+        if (!FM_IN(r * S + 2 * c2 + e < cap.n && se < T, cap.err)) continue;
         if (se < 0) {
           *de = raw_zero<Raw>();
         } else if constexpr (sizeof(Raw) == 4) {
@@ -267,7 +288,8 @@ __device__ __noinline__ void stage_rows_padded(const Raw* __restrict__ src, long
 // The caller commits the group, waits for it and then synchronises the CTA.
 template <typename Raw, int NWARPS>
 __device__ __forceinline__ void stage_tile(const Raw* __restrict__ src, long long T, long long gstart, int rows,
-                                           int hop, int S, Raw* dst, int warp, int lane, const PadSpec& ps) {
+                                           int hop, int S, Raw* dst, int warp, int lane, const PadSpec& ps,
+                                           Cap cap) {
   const bool interior = gstart >= 0 && gstart + (long long)rows * hop <= T;
   const bool aligned = ((reinterpret_cast<uintptr_t>(src + gstart)) % (2 * sizeof(Raw))) == 0;
   const int pairs = hop / 2;
@@ -275,11 +297,13 @@ __device__ __forceinline__ void stage_tile(const Raw* __restrict__ src, long lon
     for (int r = warp; r < rows; r += NWARPS) {
       const Raw* s = src + gstart + (long long)r * hop;
       Raw* d = dst + r * S;
-      for (int c2 = lane; c2 < pairs; c2 += 32) cp_async<2 * sizeof(Raw)>(d + 2 * c2, s + 2 * c2);
+      for (int c2 = lane; c2 < pairs; c2 += 32)
+        if (FM_IN(r * S + 2 * c2 + 1 < cap.n && gstart + (long long)r * hop + 2 * c2 + 1 < T, cap.err))
+          cp_async<2 * sizeof(Raw)>(d + 2 * c2, s + 2 * c2);
     }
     return;
   }
-  stage_rows_padded<Raw>(src, T, gstart, rows, hop, S, dst, warp, NWARPS, lane, ps);
+  stage_rows_padded<Raw>(src, T, gstart, rows, hop, S, dst, warp, NWARPS, lane, ps, cap);
 }
 
 // Staging for odd hops, where rows of one hop cannot keep sample pairs
@@ -292,13 +316,14 @@ __device__ __forceinline__ void stage_tile(const Raw* __restrict__ src, long lon
 // synchronises as for stage_tile.
 template <typename Raw>
 __device__ __noinline__ void stage_run(const Raw* __restrict__ src, long long T, long long gstart, int len, Raw* dst,
-                                       int tid, int nthreads, PadSpec ps) {
+                                       int tid, int nthreads, PadSpec ps, Cap cap) {
   const long long end = T + ps.zpad + ps.cpad;  // one past the padded signal
   if constexpr (sizeof(Raw) == 2) {
     const bool pairs_ok = gstart >= 0 && gstart + len <= T && (reinterpret_cast<uintptr_t>(src + gstart) & 3) == 0;
     if (pairs_ok) {
-      for (int i = 2 * tid; i + 1 < len; i += 2 * nthreads) cp_async<4>(dst + i, src + gstart + i);
-      if ((len & 1) && tid == 0) dst[len - 1] = load_one(src + gstart + len - 1);
+      for (int i = 2 * tid; i + 1 < len; i += 2 * nthreads)
+        if (FM_IN(i + 1 < cap.n, cap.err)) cp_async<4>(dst + i, src + gstart + i);
+      if ((len & 1) && tid == 0 && FM_IN(len - 1 < cap.n, cap.err)) dst[len - 1] = load_one(src + gstart + len - 1);
       return;
     }
   }
@@ -306,6 +331,7 @@ __device__ __noinline__ void stage_run(const Raw* __restrict__ src, long long T,
     const long long s = gstart + i;
     if (s >= end) break;  // s only grows with i
     const long long se = (s >= 0 && s < T) ? s : padded_source(s, T, ps);
+    if (!FM_IN(i < cap.n && se < T, cap.err)) continue;
     if (se < 0) {
       dst[i] = raw_zero<Raw>();
     } else if constexpr (sizeof(Raw) == 4) {
@@ -318,23 +344,29 @@ __device__ __noinline__ void stage_run(const Raw* __restrict__ src, long long T,
 
 // Pass 1 for role p and frame g: windowed Q-point DFT of z[p + P q] and the
 // four-step twiddle W_M^{p k2}; writes row g of the exchange buffer at
-// [k2 * P + p].
+// [k2 * P + p]. frame_off / xoff: the frame's and the row's offsets in the
+// staging and exchange buffers (for the debug build's index checks).
 template <int P, int Q, bool ODD, typename Raw>
 __device__ __forceinline__ void pass1(const Raw* __restrict__ frame_base, const float4* __restrict__ s_p1,
-                                      const float2* __restrict__ s_twh, float2* xrow, int p) {
+                                      const float2* __restrict__ s_twh, float2* xrow, int p, int frame_off,
+                                      Cap in_cap, int xoff, Cap x_cap) {
   float2 z[Q];
   const float4* tab = s_p1 + p * Q;
 #pragma unroll
   for (int q = 0; q < Q; ++q) {
     const float4 e = tab[q];
-    const Raw* src = frame_base + __float_as_int(e.z);
-    const float2 v = ODD ? load_pair_odd(src) : load_pair(src);
+    const int o = __float_as_int(e.z);
+    const Raw* src = frame_base + o;
+    float2 v = make_float2(0.0f, 0.0f);
+    if (FM_IN(frame_off + o >= 0 && frame_off + o + 1 < in_cap.n, in_cap.err))
+      v = ODD ? load_pair_odd(src) : load_pair(src);
     z[q] = make_float2(v.x * e.x, v.y * e.y);
   }
   dft<Q>(z);
-  xrow[p] = z[0];
+  if (FM_IN(xoff + p < x_cap.n, x_cap.err)) xrow[p] = z[0];
 #pragma unroll
-  for (int k2 = 1; k2 < Q; ++k2) xrow[k2 * P + p] = cmul(z[k2], s_twh[p * k2]);
+  for (int k2 = 1; k2 < Q; ++k2)
+    if (FM_IN(xoff + k2 * P + p < x_cap.n, x_cap.err)) xrow[k2 * P + p] = cmul(z[k2], s_twh[p * k2]);
 }
 
 // Copy `bytes` (a multiple of 8, both ends 8-byte aligned) from global to
@@ -400,7 +432,7 @@ __device__ __forceinline__ void split_pair(float2 zk, float2 zm, float2 w, float
 // buffer: the barrier inside separates all reads from all writes).
 template <int N, int P, int Q, int MODE>
 __device__ __forceinline__ void pass2_split_paired(const float2* xrow, float* prow, const float2* __restrict__ s_twf,
-                                                   int t, float pw) {
+                                                   int t, float pw, int xoff, Cap x_cap, int poff, Cap p_cap) {
   constexpr int M = N / 2;
   static_assert(Q == 2 * P && P % 2 == 0, "paired split needs Q = 2P with P even");
   const int kA = t;                      // 0 for role 0
@@ -408,8 +440,8 @@ __device__ __forceinline__ void pass2_split_paired(const float2* xrow, float* pr
   float2 a[P], b[P];
 #pragma unroll
   for (int p = 0; p < P; ++p) {
-    a[p] = xrow[kA * P + p];
-    b[p] = xrow[kB * P + p];
+    a[p] = get(xrow, xoff, kA * P + p, x_cap);
+    b[p] = get(xrow, xoff, kB * P + p, x_cap);
   }
   dft<P>(a);  // a[k1] = Z[kA + Q k1]
   dft<P>(b);  // b[k1] = Z[kB + Q k1]
@@ -421,8 +453,8 @@ __device__ __forceinline__ void pass2_split_paired(const float2* xrow, float* pr
       const int k = t + Q * k1;
       float lo, hi;
       split_pair<MODE>(a[k1], b[P - 1 - k1], s_twf[k], pw, lo, hi);
-      prow[k] = lo;
-      prow[M - k] = hi;
+      put(prow, poff, k, lo, p_cap);
+      put(prow, poff, M - k, hi, p_cap);
     }
   } else {
     // k = Q k1 pairs with Q (P - k1); k1 = 0 gives X[0] and X[M]
@@ -431,8 +463,8 @@ __device__ __forceinline__ void pass2_split_paired(const float2* xrow, float* pr
       const int k = Q * k1;
       float lo, hi;
       split_pair<MODE>(a[k1], a[(P - k1) % P], s_twf[k], pw, lo, hi);
-      prow[k] = lo;
-      prow[M - k] = hi;
+      put(prow, poff, k, lo, p_cap);
+      put(prow, poff, M - k, hi, p_cap);
     }
     // k = Q/2 + Q k1 pairs with Q/2 + Q (P - 1 - k1)
 #pragma unroll
@@ -440,8 +472,8 @@ __device__ __forceinline__ void pass2_split_paired(const float2* xrow, float* pr
       const int k = Q / 2 + Q * k1;
       float lo, hi;
       split_pair<MODE>(b[k1], b[P - 1 - k1], s_twf[k], pw, lo, hi);
-      prow[k] = lo;
-      prow[M - k] = hi;
+      put(prow, poff, k, lo, p_cap);
+      put(prow, poff, M - k, hi, p_cap);
     }
   }
 }
@@ -450,41 +482,44 @@ __device__ __forceinline__ void pass2_split_paired(const float2* xrow, float* pr
 // back through shared memory, and role t then splits the pairs k = t + P j.
 template <int N, int P, int Q, int MODE>
 __device__ __forceinline__ void pass2_split_exchange(float2* xrow, float* prow, const float2* __restrict__ s_twf,
-                                                     int t, float pw) {
+                                                     int t, float pw, int xoff, Cap x_cap, int poff, Cap p_cap) {
   constexpr int M = N / 2;
   constexpr int PAIRS = M / 2 + 1;  // k = 0 .. M/2
   constexpr int PPR = (PAIRS + P - 1) / P;
   static_assert(Q == P, "exchange split is for Q = P");
   float2 y[P];
 #pragma unroll
-  for (int p = 0; p < P; ++p) y[p] = xrow[t * P + p];
+  for (int p = 0; p < P; ++p) y[p] = get(xrow, xoff, t * P + p, x_cap);
   dft<P>(y);
   __syncthreads();
 #pragma unroll
-  for (int k1 = 0; k1 < P; ++k1) xrow[t + Q * k1] = y[k1];
+  for (int k1 = 0; k1 < P; ++k1) put(xrow, xoff, t + Q * k1, y[k1], x_cap);
   __syncthreads();
   float lo[PPR], hi[PPR];
 #pragma unroll
   for (int i = 0; i < PPR; ++i) {
     const int k = t + i * P;
     lo[i] = hi[i] = 0.0f;
-    if (k <= M / 2) split_pair<MODE>(xrow[k], xrow[k == 0 ? 0 : M - k], s_twf[k], pw, lo[i], hi[i]);
+    if (k <= M / 2)
+      split_pair<MODE>(get(xrow, xoff, k, x_cap), get(xrow, xoff, k == 0 ? 0 : M - k, x_cap), s_twf[k], pw, lo[i],
+                       hi[i]);
   }
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < PPR; ++i) {
     const int k = t + i * P;
     if (k <= M / 2) {
-      prow[k] = lo[i];
-      prow[M - k] = hi[i];
+      put(prow, poff, k, lo[i], p_cap);
+      put(prow, poff, M - k, hi[i], p_cap);
     }
   }
 }
 
 template <int N, int P, int Q, int MODE>
-__device__ __forceinline__ void pass2_split(float2* xrow, float* prow, const float2* s_twf, int t, float pw) {
-  if constexpr (Q == 2 * P) pass2_split_paired<N, P, Q, MODE>(xrow, prow, s_twf, t, pw);
-  else pass2_split_exchange<N, P, Q, MODE>(xrow, prow, s_twf, t, pw);
+__device__ __forceinline__ void pass2_split(float2* xrow, float* prow, const float2* s_twf, int t, float pw, int xoff,
+                                            Cap x_cap, int poff, Cap p_cap) {
+  if constexpr (Q == 2 * P) pass2_split_paired<N, P, Q, MODE>(xrow, prow, s_twf, t, pw, xoff, x_cap, poff, p_cap);
+  else pass2_split_exchange<N, P, Q, MODE>(xrow, prow, s_twf, t, pw, xoff, x_cap, poff, p_cap);
 }
 
 __device__ __forceinline__ void store_out(float* o, float v) { *o = v; }
@@ -492,10 +527,13 @@ __device__ __forceinline__ void store_out(__half* o, float v) { *o = __float2hal
 
 // Sparse mel projection: lane = frame, G lanes per mel, warp-uniform filter
 // rows read as broadcasts; stores of consecutive frames are coalesced.
+// p_cap: the power tile's floats; nnz: the filter weights; out_left: output
+// elements from out_tile to the end of the output (debug-build checks).
 template <int G, int NWARPS, int PS, typename OutT>
 __device__ __forceinline__ void mel_project(const float* s_pw, const int4* __restrict__ s_mel,
                                             const float* __restrict__ s_mw, OutT* out_tile, int n_valid,
-                                            int n_mels, long long n_frames, int warp, int lane) {
+                                            int n_mels, long long n_frames, int warp, int lane, Cap p_cap,
+                                            int nnz, long long out_left) {
   constexpr int SUBS = 32 / G;
   const int gg = lane % G, sub = lane / G;
   const float* prow = s_pw + gg * PS;
@@ -507,8 +545,11 @@ __device__ __forceinline__ void mel_project(const float* s_pw, const int4* __res
     const float* wr = s_mw + md.z;
     float acc = 0.0f;
 #pragma unroll 4
-    for (int j = 0; j < md.y; ++j) acc = fmaf(wr[j], pr[j], acc);
-    if (valid) store_out(o + (long long)m * n_frames, acc);
+    for (int j = 0; j < md.y; ++j)
+      if (FM_IN(gg * PS + md.x + j >= 0 && gg * PS + md.x + j < p_cap.n && md.z + j >= 0 && md.z + j < nnz,
+                p_cap.err))
+        acc = fmaf(wr[j], pr[j], acc);
+    if (valid && FM_IN(gg + (long long)m * n_frames < out_left, p_cap.err)) store_out(o + (long long)m * n_frames, acc);
   }
 }
 
@@ -538,15 +579,20 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
   const TileSplitter split(prm.tiles_per_signal);
   const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
   auto in_buf = [&](int i) { return reinterpret_cast<Raw*>(smem + lay.in_tile + (size_t)i * lay.in_tile_bytes); };
+  // buffer sizes for the debug build's index checks
+  const Cap in_cap = {(int)(lay.in_tile_bytes / sizeof(Raw)), prm.err};
+  const Cap x_cap = {G * GS, prm.err}, p_cap = {G * PS, prm.err};
+  const long long out_total = prm.B * (long long)prm.n_mels * prm.n_frames;
   auto stage = [&](long long tile, int buf) {
     long long b;
     int tt;
     split(tile, b, tt);
     const long long t0 = (long long)tt * G;
     if constexpr (ODD)  // rows of one odd hop, back to back (S == hop)
-      stage_run<Raw>(in + b * T, T, t0 * hop - prm.lead, rows * hop, in_buf(buf), tid, THREADS, pads);
+      stage_run<Raw>(in + b * T, T, t0 * hop - prm.lead, rows * hop, in_buf(buf), tid, THREADS, pads, in_cap);
     else
-      stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.lead, rows, hop, S, in_buf(buf), warp, lane, pads);
+      stage_tile<Raw, NWARPS>(in + b * T, T, t0 * hop - prm.lead, rows, hop, S, in_buf(buf), warp, lane, pads,
+                              in_cap);
     cp_async_commit();
   };
 
@@ -560,15 +606,15 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
     if (NBUF == 2 && next < prm.total_tiles) stage(next, buf ^ 1);
 
     float2* xrow = s_x + g * GS;
-    pass1<P, Q, ODD, Raw>(in_buf(buf) + g * S, s_p1, s_twh, xrow, role);
+    pass1<P, Q, ODD, Raw>(in_buf(buf) + g * S, s_p1, s_twh, xrow, role, g * S, in_cap, g * GS, x_cap);
     __syncthreads();
     if (NBUF == 1 && next < prm.total_tiles) stage(next, 0);  // pass 1 was the last reader
 
     float* prow = s_pw + g * PS;
     switch (prm.power_mode) {
-      case 0: pass2_split<N, P, Q, 0>(xrow, prow, s_twf, role, prm.power); break;
-      case 1: pass2_split<N, P, Q, 1>(xrow, prow, s_twf, role, prm.power); break;
-      default: pass2_split<N, P, Q, 2>(xrow, prow, s_twf, role, prm.power); break;
+      case 0: pass2_split<N, P, Q, 0>(xrow, prow, s_twf, role, prm.power, g * GS, x_cap, g * PS, p_cap); break;
+      case 1: pass2_split<N, P, Q, 1>(xrow, prow, s_twf, role, prm.power, g * GS, x_cap, g * PS, p_cap); break;
+      default: pass2_split<N, P, Q, 2>(xrow, prow, s_twf, role, prm.power, g * GS, x_cap, g * PS, p_cap); break;
     }
     __syncthreads();
 
@@ -580,10 +626,10 @@ __device__ __forceinline__ void run_tiles(const KernelParams& prm, unsigned char
     const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
     if (prm.out_dtype == FM_F32)
       mel_project<G, NWARPS, PS>(s_pw, s_mel, s_mw, static_cast<float*>(prm.out) + obase, n_valid, prm.n_mels,
-                                 prm.n_frames, warp, lane);
+                                 prm.n_frames, warp, lane, p_cap, prm.nnz, out_total - obase);
     else
       mel_project<G, NWARPS, PS>(s_pw, s_mel, s_mw, static_cast<__half*>(prm.out) + obase, n_valid, prm.n_mels,
-                                 prm.n_frames, warp, lane);
+                                 prm.n_frames, warp, lane, p_cap, prm.nnz, out_total - obase);
     if (NBUF == 2) buf ^= 1;
     // The next iteration's barrier orders these power-tile reads before the
     // next pass 1 overwrites the exchange buffer.

@@ -54,8 +54,31 @@ __host__ __device__ constexpr int big_frame_stride(int M) { return M + (M >> 4) 
 __host__ __device__ constexpr size_t big_smem_bytes(int n_fft) {
   return sizeof(float2) * (size_t)big_frames(n_fft) * (size_t)big_frame_stride(n_fft / 2);
 }
+// Twiddles from shared memory in two levels, W^t = W^(t mod 64) W^(64 floor(t / 64)):
+// rows of 64 fine and M/64 (+1) coarse factors of W_M (the passes) and of W_N
+// (the split), gathered from the plan's full tables when a CTA starts. A full
+// table (64 KB at n_fft 16384) would not stay in L1 beside the transform.
+constexpr int kBigTwFine = 64;
+__host__ __device__ constexpr int big_tw_count(int M) { return 2 * kBigTwFine + M / kBigTwFine + M / kBigTwFine + 1; }
+
+// Shared memory of the large-transform kernel after the transform buffer:
+// the twiddle rows, the filterbank (descriptors and weights) and, when one
+// tile's span fits, the staging buffer of the next tile's samples.
+struct BigLayout {
+  size_t tw, mel, mw, st;
+};
+__host__ __device__ inline BigLayout big_layout(int n_fft, int n_mels, int nnz) {
+  BigLayout L;
+  size_t o = big_smem_bytes(n_fft);
+  L.tw = o;   o = align16(o + sizeof(float2) * big_tw_count(n_fft / 2));
+  L.mel = o;  o = align16(o + sizeof(int4) * n_mels);
+  L.mw = o;   o = align16(o + sizeof(float) * (nnz > 0 ? nnz : 1));
+  L.st = o;
+  return L;
+}
+
 // Samples one tile's frames cover, (F - 1) hop + n_fft: the span the kernel
-// prefetches into a staging buffer behind the transform buffer when it fits
+// prefetches into a staging buffer after the tables when it fits
 // (KernelParams::big_span), 16-byte aligned.
 __host__ __device__ constexpr long long big_span(int n_fft, int hop) {
   return (long long)(big_frames(n_fft) - 1) * hop + n_fft;
@@ -85,7 +108,8 @@ __device__ __forceinline__ float big_sample(const Raw* __restrict__ sig, long lo
 // latency rather than one per few pairs.
 template <int N, typename Raw>
 __device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ sig, long long T, long long s0,
-                                         int hop, const float2* __restrict__ win2, const PadSpec& ps, int tid) {
+                                         int hop, const float2* __restrict__ win2, const PadSpec& ps, int tid,
+                                         Cap x_cap) {
   constexpr int M = N / 2, F = big_frames(N), FS = big_frame_stride(M);
   constexpr int PER = F * M / kBigThreads;
   static_assert((F * M) % kBigThreads == 0, "pairs must divide evenly over the threads");
@@ -96,7 +120,8 @@ __device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ si
     const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
     const long long s = s0 + (long long)f * hop + 2 * n;
     if (interior) {
-      v[i] = make_float2(raw_to_float(sig[s]), raw_to_float(sig[s + 1]));
+      v[i] = FM_IN(s >= 0 && s + 1 < T, x_cap.err) ? make_float2(raw_to_float(sig[s]), raw_to_float(sig[s + 1]))
+                                                   : make_float2(0.0f, 0.0f);
     } else {
       v[i] = make_float2(big_sample(sig, T, s, ps), big_sample(sig, T, s + 1, ps));
     }
@@ -105,7 +130,7 @@ __device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ si
   for (int i = 0; i < PER; ++i) {
     const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
     const float2 w = __ldg(win2 + n);
-    s_x[f * FS + big_phys(n)] = make_float2(v[i].x * w.x, v[i].y * w.y);
+    put(s_x, 0, f * FS + big_phys(n), make_float2(v[i].x * w.x, v[i].y * w.y), x_cap);
   }
 }
 
@@ -113,7 +138,7 @@ __device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ si
 // (st[i] = the sample at padded position s0 + i, see stage_run).
 template <int N, typename Raw>
 __device__ __forceinline__ void big_load_staged(float2* s_x, const Raw* st, int hop, const float2* __restrict__ win2,
-                                                int tid) {
+                                                int tid, Cap x_cap, Cap st_cap) {
   constexpr int M = N / 2, F = big_frames(N), FS = big_frame_stride(M);
   constexpr int PER = F * M / kBigThreads;
 #pragma unroll 8
@@ -121,14 +146,22 @@ __device__ __forceinline__ void big_load_staged(float2* s_x, const Raw* st, int 
     const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
     const Raw* p = st + f * hop + 2 * n;
     const float2 w = __ldg(win2 + n);
-    s_x[f * FS + big_phys(n)] = make_float2(raw_to_float(p[0]) * w.x, raw_to_float(p[1]) * w.y);
+    const float2 v = FM_IN(f * hop + 2 * n + 1 < st_cap.n, st_cap.err) ? make_float2(raw_to_float(p[0]), raw_to_float(p[1]))
+                                                                      : make_float2(0.0f, 0.0f);
+    put(s_x, 0, f * FS + big_phys(n), make_float2(v.x * w.x, v.y * w.y), x_cap);
   }
 }
 
 // One radix-R autosorting pass over the F frames (Ns = product of the
 // earlier radices).
+// W_M^t from the two twiddle rows of W_M (fine: t mod 64, coarse: t / 64)
+template <int M>
+__device__ __forceinline__ float2 big_tw(const float2* s_tw, int t) {
+  return cmul(s_tw[t & (kBigTwFine - 1)], s_tw[kBigTwFine + (t >> 6)]);
+}
+
 template <int M, int F, int R, int NS>
-__device__ __forceinline__ void big_pass(float2* s_x, const float2* __restrict__ tw_m, int tid) {
+__device__ __forceinline__ void big_pass(float2* s_x, const float2* s_tw, int tid, Cap x_cap) {
   constexpr int J = M / R;  // butterflies per frame
   constexpr int FS = big_frame_stride(M);
   static_assert((F * J) % kBigThreads == 0, "butterflies must divide evenly over the threads");
@@ -140,11 +173,11 @@ __device__ __forceinline__ void big_pass(float2* s_x, const float2* __restrict__
     const int f = task / J, j = task % J;
     const float2* xf = s_x + f * FS;
 #pragma unroll
-    for (int r = 0; r < R; ++r) v[t][r] = xf[big_phys(j + r * J)];
+    for (int r = 0; r < R; ++r) v[t][r] = get<float2>(xf, f * FS, big_phys(j + r * J), x_cap);
     if constexpr (NS > 1) {
       const int e = (j % NS) * (M / (NS * R));  // W_{Ns R}^{(j mod Ns) r} = W_M^{e r}, e r < M
 #pragma unroll
-      for (int r = 1; r < R; ++r) v[t][r] = cmul(v[t][r], __ldg(tw_m + e * r));
+      for (int r = 1; r < R; ++r) v[t][r] = cmul(v[t][r], big_tw<M>(s_tw, e * r));
     }
     dft<R>(v[t]);
   }
@@ -156,7 +189,7 @@ __device__ __forceinline__ void big_pass(float2* s_x, const float2* __restrict__
     float2* xf = s_x + f * FS;
     const int d = (j / NS) * NS * R + (j % NS);
 #pragma unroll
-    for (int r = 0; r < R; ++r) xf[big_phys(d + r * NS)] = v[t][r];
+    for (int r = 0; r < R; ++r) put(xf, f * FS, big_phys(d + r * NS), v[t][r], x_cap);
   }
   __syncthreads();
 }
@@ -164,8 +197,8 @@ __device__ __forceinline__ void big_pass(float2* s_x, const float2* __restrict__
 // Real-FFT split and |X|^p for k = 0 .. M/2 of every frame, into the power
 // tile (float rows of M + 1, aliasing the buffer: all reads, barrier, writes).
 template <int M, int F, int MODE>
-__device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2* __restrict__ tw_n, float pw,
-                                          int tid) {
+__device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2* s_twn, float pw, int tid,
+                                          Cap x_cap, Cap p_cap) {
   constexpr int FS = big_frame_stride(M), PS = M + 1;
   constexpr int PAIRS = M / 2 + 1, TOTAL = F * PAIRS;
   constexpr int PER = (TOTAL + kBigThreads - 1) / kBigThreads;
@@ -176,9 +209,11 @@ __device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2
     lo[i] = hi[i] = 0.0f;
     if (task < TOTAL) {
       const int f = task / PAIRS, k = task % PAIRS;
-      const float2 zk = s_x[f * FS + big_phys(k)];
-      const float2 zm = s_x[f * FS + big_phys((M - k) & (M - 1))];
-      split_pair<MODE>(zk, zm, __ldg(tw_n + k), pw, lo[i], hi[i]);
+      const float2 zk = get<float2>(s_x, 0, f * FS + big_phys(k), x_cap);
+      const float2 zm = get<float2>(s_x, 0, f * FS + big_phys((M - k) & (M - 1)), x_cap);
+      // W_N^k from the two twiddle rows of W_N
+      const float2 w = cmul(s_twn[k & (kBigTwFine - 1)], s_twn[kBigTwFine + (k >> 6)]);
+      split_pair<MODE>(zk, zm, w, pw, lo[i], hi[i]);
     }
   }
   __syncthreads();
@@ -187,8 +222,8 @@ __device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2
     const int task = tid + i * kBigThreads;
     if (task < TOTAL) {
       const int f = task / PAIRS, k = task % PAIRS;
-      s_pw[f * PS + k] = lo[i];
-      s_pw[f * PS + M - k] = hi[i];
+      put(s_pw, 0, f * PS + k, lo[i], p_cap);
+      put(s_pw, 0, f * PS + M - k, hi[i], p_cap);
     }
   }
   __syncthreads();
@@ -209,13 +244,24 @@ __device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned 
   const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
   // With a staging buffer (prm.big_span > 0), the next tile's samples are
   // prefetched by cp.async while this tile's transform runs.
-  Raw* s_st = reinterpret_cast<Raw*>(smem + big_smem_bytes(N));
+  const BigLayout lay = big_layout(N, prm.n_mels, prm.nnz);
+  const float2* s_tw = reinterpret_cast<const float2*>(smem + lay.tw);  // W_M rows, then W_N rows
+  const float2* s_twn = s_tw + kBigTwFine + M / kBigTwFine;
+  const int4* s_mel = reinterpret_cast<const int4*>(smem + lay.mel);
+  const float* s_mw = reinterpret_cast<const float*>(smem + lay.mw);
+  Raw* s_st = reinterpret_cast<Raw*>(smem + lay.st);
   const int span = prm.big_span;
+  // buffer sizes for the debug build's index checks (the staging buffer holds
+  // span samples, rounded up to 16 bytes)
+  const Cap x_cap = {F * big_frame_stride(M), prm.err}, p_cap = {F * (M + 1), prm.err};
+  const Cap st_cap = {span, prm.err};
+  const long long out_total = prm.B * (long long)prm.n_mels * prm.n_frames;
   auto prefetch = [&](long long t) {
     long long bb;
     int tq;
     split(t, bb, tq);
-    stage_run<Raw>(in + bb * T, T, (long long)tq * F * prm.hop - prm.lead, span, s_st, tid, kBigThreads, pads);
+    stage_run<Raw>(in + bb * T, T, (long long)tq * F * prm.hop - prm.lead, span, s_st, tid, kBigThreads, pads,
+                   st_cap);
     cp_async_commit();
   };
   if (span > 0 && (long long)blockIdx.x < prm.total_tiles) prefetch(blockIdx.x);
@@ -227,36 +273,55 @@ __device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned 
     if (span > 0) cp_async_wait_all();  // this thread's copies of the tile have landed
     __syncthreads();  // the previous tile's mel reads are done; the staged tile is visible
     if (span > 0)
-      big_load_staged<N, Raw>(s_x, s_st, prm.hop, win2, tid);
+      big_load_staged<N, Raw>(s_x, s_st, prm.hop, win2, tid, x_cap, st_cap);
     else
-      big_load<N, Raw>(s_x, in + b * T, T, (long long)t0 * prm.hop - prm.lead, prm.hop, win2, pads, tid);
+      big_load<N, Raw>(s_x, in + b * T, T, (long long)t0 * prm.hop - prm.lead, prm.hop, win2, pads, tid, x_cap);
     __syncthreads();
     if (span > 0 && tile + gridDim.x < prm.total_tiles) prefetch(tile + gridDim.x);  // staging read: reuse it
-    big_pass<M, F, R0, 1>(s_x, prm.tw_half, tid);
-    big_pass<M, F, R1, R0>(s_x, prm.tw_half, tid);
-    big_pass<M, F, R2, R0 * R1>(s_x, prm.tw_half, tid);
+    big_pass<M, F, R0, 1>(s_x, s_tw, tid, x_cap);
+    big_pass<M, F, R1, R0>(s_x, s_tw, tid, x_cap);
+    big_pass<M, F, R2, R0 * R1>(s_x, s_tw, tid, x_cap);
     switch (prm.power_mode) {
-      case 0: big_split<M, F, 0>(s_x, s_pw, prm.tw_full, prm.power, tid); break;
-      case 1: big_split<M, F, 1>(s_x, s_pw, prm.tw_full, prm.power, tid); break;
-      default: big_split<M, F, 2>(s_x, s_pw, prm.tw_full, prm.power, tid); break;
+      case 0: big_split<M, F, 0>(s_x, s_pw, s_twn, prm.power, tid, x_cap, p_cap); break;
+      case 1: big_split<M, F, 1>(s_x, s_pw, s_twn, prm.power, tid, x_cap, p_cap); break;
+      default: big_split<M, F, 2>(s_x, s_pw, s_twn, prm.power, tid, x_cap, p_cap); break;
     }
     const int n_valid = min(F, prm.n_frames - t0);
     const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
     if (prm.out_dtype == FM_F32)
-      mel_project<F, NWARPS, M + 1>(s_pw, prm.mel, prm.mel_w, static_cast<float*>(prm.out) + obase, n_valid,
-                                    prm.n_mels, prm.n_frames, warp, lane);
+      mel_project<F, NWARPS, M + 1>(s_pw, s_mel, s_mw, static_cast<float*>(prm.out) + obase, n_valid,
+                                    prm.n_mels, prm.n_frames, warp, lane, p_cap, prm.nnz, out_total - obase);
     else
-      mel_project<F, NWARPS, M + 1>(s_pw, prm.mel, prm.mel_w, static_cast<__half*>(prm.out) + obase, n_valid,
-                                    prm.n_mels, prm.n_frames, warp, lane);
+      mel_project<F, NWARPS, M + 1>(s_pw, s_mel, s_mw, static_cast<__half*>(prm.out) + obase, n_valid,
+                                    prm.n_mels, prm.n_frames, warp, lane, p_cap, prm.nnz, out_total - obase);
   }
   cp_async_wait_all();  // nothing stays in flight past the end of the CTA
 }
 
 template <int N>
 __global__ void __launch_bounds__(kBigThreads, 1) mel_kernel_big(const KernelParams prm) {
+  constexpr int M = N / 2, ROWS = M / kBigTwFine;
   extern __shared__ __align__(16) unsigned char smem[];
   pdl_launch_dependents();
+  // the plan's tables, once per CTA (the grid is persistent): the twiddle rows
+  // gathered from the full W_M and W_N tables, and the filterbank
+  const BigLayout lay = big_layout(N, prm.n_mels, prm.nnz);
+  float2* s_tw = reinterpret_cast<float2*>(smem + lay.tw);
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kBigTwFine; i += kBigThreads) {
+    s_tw[i] = prm.tw_half[i];                             // W_M^i
+    s_tw[kBigTwFine + ROWS + i] = prm.tw_full[i];         // W_N^i
+  }
+  for (int i = tid; i < ROWS; i += kBigThreads) s_tw[kBigTwFine + i] = prm.tw_half[kBigTwFine * i];  // W_M^(64 i)
+  for (int i = tid; i <= ROWS; i += kBigThreads)
+    s_tw[2 * kBigTwFine + ROWS + i] = prm.tw_full[kBigTwFine * i];  // W_N^(64 i), 64 i <= M
+  copy_table_async(smem + lay.mel, prm.mel, (int)sizeof(int4) * prm.n_mels, tid, kBigThreads);
+  copy_table_async(smem + lay.mw, prm.mel_w, (int)align16(sizeof(float) * (prm.nnz > 0 ? prm.nnz : 1)), tid,
+                   kBigThreads);
+  cp_async_commit();
+  cp_async_wait_all();
   pdl_wait();  // caller buffers only after the previous kernel in the stream is done
+  // (the first barrier of the tile loop publishes the tables)
   if (prm.in_dtype == FM_F32) run_tiles_big<N, float>(prm, smem);
   else if (prm.in_dtype == FM_I16) run_tiles_big<N, short>(prm, smem);
   else run_tiles_big<N, __half>(prm, smem);

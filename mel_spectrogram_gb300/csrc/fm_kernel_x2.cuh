@@ -53,9 +53,18 @@ __device__ __forceinline__ bool group_sync_or(int id, int n, bool v) {
 // 2Pq + 2p do not depend on p, so every load is a compile-time offset from
 // base or base_o (frame g + 16 is 8 lines further). HOP = 0: lines of one hop,
 // frame g on line g, and the offsets come from the table.
+// A sample pair of the staged tile, read only if it lies inside the staging
+// area that starts at s_in (checked in the debug build).
+template <typename Raw>
+__device__ __forceinline__ float2 staged_pair(const Raw* p, const Raw* s_in, Cap cap) {
+  const long long o = p - s_in;
+  return FM_IN(o >= 0 && o + 1 < cap.n, cap.err) ? load_pair(p) : make_float2(0.0f, 0.0f);
+}
+
 template <int P, int Q, int HOP, typename Raw>
 __device__ __forceinline__ void pass1_load_x2(const Raw* __restrict__ base, const Raw* __restrict__ base_o, int S,
-                                              const float4* __restrict__ s_p1, int p, cx2 (&z)[Q]) {
+                                              const float4* __restrict__ s_p1, int p, cx2 (&z)[Q], const Raw* s_in,
+                                              Cap in_cap) {
   const float4* tab = s_p1 + p * Q;
   if constexpr (HOP > 0) {
     static_assert(HOP % (2 * P) == 0, "compile-time hop must be a multiple of 2P");
@@ -68,8 +77,8 @@ __device__ __forceinline__ void pass1_load_x2(const Raw* __restrict__ base, cons
       const int ce = j / (2 * HOP), co = (HOP + j) / (2 * HOP);  // lines crossed, even / odd g
       const Raw* b = co != ce ? base_o : base;
       const int off = j + ce * PAD;
-      const float2 va = load_pair(b + off);
-      const float2 vb = load_pair(b + off + (kX2Lanes / 2) * SC);
+      const float2 va = staged_pair(b + off, s_in, in_cap);
+      const float2 vb = staged_pair(b + off + (kX2Lanes / 2) * SC, s_in, in_cap);
       z[q].re = make_float2(va.x * w.x, vb.x * w.x);
       z[q].im = make_float2(va.y * w.y, vb.y * w.y);
     }
@@ -79,8 +88,8 @@ __device__ __forceinline__ void pass1_load_x2(const Raw* __restrict__ base, cons
     for (int q = 0; q < Q; ++q) {
       const float4 e = tab[q];
       const int off = __float_as_int(e.z);
-      const float2 va = load_pair(base + off);
-      const float2 vb = load_pair(base_b + off);
+      const float2 va = staged_pair(base + off, s_in, in_cap);
+      const float2 vb = staged_pair(base_b + off, s_in, in_cap);
       z[q].re = make_float2(va.x * e.x, vb.x * e.x);
       z[q].im = make_float2(va.y * e.y, vb.y * e.y);
     }
@@ -114,14 +123,15 @@ __device__ __forceinline__ void split_pair_x2(cx2 zk, cx2 zm, float4 w, float pw
 // Pass 2 for Q = 2P: role t >= 1 holds k2 = t and Q - t, role 0 holds k2 = 0
 // and Q/2; P-point DFTs over p give a[k1] = Z[kA + Q k1], b[k1] = Z[kB + Q k1].
 template <int P, int Q>
-__device__ __forceinline__ void pass2_x2(const float4* xq_row, int t, cx2 (&a)[P], cx2 (&b)[P]) {
+__device__ __forceinline__ void pass2_x2(const float4* xq_row, int t, cx2 (&a)[P], cx2 (&b)[P], int xoff, Cap x_cap) {
   static_assert(Q == 2 * P && P % 2 == 0, "paired split needs Q = 2P with P even");
   const int kA = t;
   const int kB = (t == 0) ? Q / 2 : Q - t;
 #pragma unroll
   for (int p = 0; p < P; ++p) {
-    a[p] = load_cx2(xq_row + kA * P + p);
-    b[p] = load_cx2(xq_row + kB * P + p);
+    const float4 va = get(xq_row, xoff, kA * P + p, x_cap), vb = get(xq_row, xoff, kB * P + p, x_cap);
+    a[p] = {make_float2(va.x, va.y), make_float2(va.z, va.w)};
+    b[p] = {make_float2(vb.x, vb.y), make_float2(vb.z, vb.w)};
   }
   dft<P>(a);
   dft<P>(b);
@@ -140,7 +150,8 @@ __device__ __forceinline__ cx2 sel(bool c, const cx2& a, const cx2& b) { return 
 // divergent paths while the other warps wait at the next barrier.
 template <int N, int P, int Q, int MODE>
 __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], float2* pw_col,
-                                         const float4* __restrict__ s_twf4, int t, float pw, bool merged) {
+                                         const float4* __restrict__ s_twf4, int t, float pw, bool merged, int poff,
+                                         Cap p_cap) {
   constexpr int M = N / 2;
   if (!merged) {
 #pragma unroll
@@ -148,8 +159,8 @@ __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], f
       const int k = t + Q * k1;
       float2 lo, hi;
       split_pair_x2<MODE>(a[k1], b[P - 1 - k1], s_twf4[k], pw, lo, hi);
-      pw_col[k * kX2Lanes] = lo;
-      pw_col[(M - k) * kX2Lanes] = hi;
+      put(pw_col, poff, k * kX2Lanes, lo, p_cap);
+      put(pw_col, poff, (M - k) * kX2Lanes, hi, p_cap);
     }
     return;
   }
@@ -174,8 +185,8 @@ __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], f
     if (j < P || r0) {
       float2 lo, hi;
       split_pair_x2<MODE>(u, v, s_twf4[k], pw, lo, hi);
-      pw_col[k * kX2Lanes] = lo;
-      pw_col[(M - k) * kX2Lanes] = hi;
+      put(pw_col, poff, k * kX2Lanes, lo, p_cap);
+      put(pw_col, poff, (M - k) * kX2Lanes, hi, p_cap);
     }
   }
 }
@@ -191,7 +202,8 @@ __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], f
 template <typename OutT>
 __device__ __forceinline__ void mel_project_x2(const unsigned char* s_pw, const int2* __restrict__ s_desc,
                                                const float4* __restrict__ s_w4, OutT* out_tile, int n_valid,
-                                               long long n_frames, int c_begin, int c_end, int lane) {
+                                               long long n_frames, int c_begin, int c_end, int lane, int pw_bytes,
+                                               int n_slots, long long out_left, unsigned* err) {
   const int l = lane & 7, h = lane >> 3;
   const unsigned char* pcol = s_pw + l * (int)sizeof(float4);
   const bool v0 = l < n_valid, v1 = l + 16 < n_valid, v2 = l + 8 < n_valid, v3 = l + 24 < n_valid;
@@ -203,12 +215,15 @@ __device__ __forceinline__ void mel_project_x2(const unsigned char* s_pw, const 
     int2 d[kX2Unroll];
     float4 w[kX2Unroll], p0[kX2Unroll], p1[kX2Unroll];
 #pragma unroll
-    for (int u = 0; u < kX2Unroll; ++u) d[u] = dp[4 * u];
+    for (int u = 0; u < kX2Unroll; ++u)
+      d[u] = FM_IN(c + u >= 0 && c + u < n_slots, err) ? dp[4 * u] : make_int2(0, -1);
 #pragma unroll
     for (int u = 0; u < kX2Unroll; ++u) {
       w[u] = wp[4 * u];
-      p0[u] = *reinterpret_cast<const float4*>(pcol + d[u].x);
-      p1[u] = *reinterpret_cast<const float4*>(pcol + d[u].x + kRow);
+      const bool in = FM_IN(d[u].x >= 0 && l * (int)sizeof(float4) + d[u].x + kRow + (int)sizeof(float4) <= pw_bytes,
+                            err);
+      p0[u] = in ? *reinterpret_cast<const float4*>(pcol + d[u].x) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      p1[u] = in ? *reinterpret_cast<const float4*>(pcol + d[u].x + kRow) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
 #pragma unroll
     for (int u = 0; u < kX2Unroll; ++u) {
@@ -218,11 +233,12 @@ __device__ __forceinline__ void mel_project_x2(const unsigned char* s_pw, const 
       a01 = fma2(w1, make_float2(p1[u].x, p1[u].y), a01);
       a23 = fma2(w1, make_float2(p1[u].z, p1[u].w), a23);
       if (d[u].y >= 0) {
-        OutT* o = out_tile + (long long)d[u].y * n_frames + l;
-        if (v0) store_out(o, a01.x);
-        if (v1) store_out(o + 16, a01.y);
-        if (v2) store_out(o + 8, a23.x);
-        if (v3) store_out(o + 24, a23.y);
+        const long long oi = (long long)d[u].y * n_frames + l;  // element offset from out_tile
+        OutT* o = out_tile + oi;
+        if (v0 && FM_IN(oi < out_left, err)) store_out(o, a01.x);
+        if (v1 && FM_IN(oi + 16 < out_left, err)) store_out(o + 16, a01.y);
+        if (v2 && FM_IN(oi + 8 < out_left, err)) store_out(o + 8, a23.x);
+        if (v3 && FM_IN(oi + 24 < out_left, err)) store_out(o + 24, a23.y);
         a01 = make_float2(0.0f, 0.0f);
         a23 = make_float2(0.0f, 0.0f);
       }
@@ -277,7 +293,8 @@ struct X2Staging {
 // the lines, each sample by one 4-byte cp.async (f32 only).
 template <typename Raw>
 __device__ __forceinline__ void stage_lines_reflect(const Raw* __restrict__ sig, long long T, long long gstart,
-                                                    int r0, int r1, int L, int S, int cpad, Raw* dst, int lane) {
+                                                    int r0, int r1, int L, int S, int cpad, Raw* dst, int lane,
+                                                    Cap cap) {
   static_assert(sizeof(Raw) == 4, "4-byte samples only");
   const long long base = gstart + (long long)r0 * L;
   const int n = (r1 - r0) * L;
@@ -290,7 +307,7 @@ __device__ __forceinline__ void stage_lines_reflect(const Raw* __restrict__ sig,
     for (int col = lane; col < L && i0 + col < c; col += 32) {
       const int i = i0 + col;
       const long long src = i < a ? -(base + i) : (i < b ? base + i : 2 * T - 2 - (base + i));
-      cp_async<4>(d + col, sig + src);
+      if (FM_IN((r0 + r) * S + col < cap.n && src >= 0 && src < T, cap.err)) cp_async<4>(d + col, sig + src);
     }
   }
 }
@@ -331,6 +348,7 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
   // pairwise cp.async)
   const bool plain_reflect = sizeof(Raw) == 4 && prm.zpad == 0 && prm.pad_mode == FM_PAD_REFLECT;
   int2* slots = reinterpret_cast<int2*>(smem + lay.slots);
+  const Cap in_cap = {(int)(lay.in_tile_bytes / sizeof(Raw)), prm.err};  // one group's staging area
   auto stage = [&](int g, long long tile, int k) {
     long long b;
     int tt;
@@ -354,7 +372,14 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     if (!tma_ok || r_lo >= r_hi) r_lo = r_hi = 0;
     // an interior tile whose rows all lie in the tensor map: one tensor copy
     const int y0 = tt * (kX2Frames / X2Staging<N, HOP, Raw>::KH) - y_lead;
-    const bool one_copy = prm.tmap_ok && y0 >= 0 && y0 + rows <= prm.tmap_rows && (smem_addr(dst) & 127u) == 0;
+    bool one_copy = prm.tmap_ok && y0 >= 0 && y0 + rows <= prm.tmap_rows && (smem_addr(dst) & 127u) == 0;
+    // debug build: a copy that would not fit the staging area is not issued
+    // (and its bytes are not expected), so the checks never leave a wait open
+    if (one_copy && !FM_IN(st.rows * st.S <= in_cap.n, prm.err)) one_copy = false;
+    if (r_hi > r_lo && !FM_IN((r_hi - 1) * st.S + L <= in_cap.n && gstart + (long long)r_lo * L >= 0 &&
+                                  gstart + (long long)r_hi * L <= T,
+                              prm.err))
+      r_lo = r_hi = 0;
     int r_stop = r_end;
     if (one_copy) r_lo = r_hi = r_stop = 0;
     // the consumers' generic accesses of the area were ordered before this
@@ -377,15 +402,16 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     const bool mirror = plain_reflect && (gstart < 0 || avail < span);
     if constexpr (sizeof(Raw) == 4) {
       if (mirror) {
-        if (r_lo > 0) stage_lines_reflect<Raw>(sig, T, gstart, 0, r_lo, L, st.S, prm.cpad, dst, lane);
-        if (r_stop > r_tail) stage_lines_reflect<Raw>(sig, T, gstart, r_tail, r_stop, L, st.S, prm.cpad, dst, lane);
+        if (r_lo > 0) stage_lines_reflect<Raw>(sig, T, gstart, 0, r_lo, L, st.S, prm.cpad, dst, lane, in_cap);
+        if (r_stop > r_tail)
+          stage_lines_reflect<Raw>(sig, T, gstart, r_tail, r_stop, L, st.S, prm.cpad, dst, lane, in_cap);
       }
     }
     if (!mirror) {
-      if (r_lo > 0) stage_tile<Raw, 1>(sig, T, gstart, r_lo, L, st.S, dst, 0, lane, pads);
+      if (r_lo > 0) stage_tile<Raw, 1>(sig, T, gstart, r_lo, L, st.S, dst, 0, lane, pads, in_cap);
       if (r_stop > r_tail)
         stage_tile<Raw, 1>(sig, T, gstart + (long long)r_tail * L, r_stop - r_tail, L, st.S, dst + r_tail * st.S,
-                           0, lane, pads);
+                           0, lane, pads, Cap{in_cap.n - r_tail * st.S, in_cap.err});
     }
     // each lane's element copies arrive on the group's barrier when they land,
     // so the warp goes on to the next group instead of waiting for DRAM here
@@ -475,6 +501,12 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
   float4* xq_row = s_xq + g * GS4;
   const float4* tw = s_twh4 + role * Q;  // this role's W_M^{p k2}, k2 < Q
   unsigned phase = 0u;
+  // buffer sizes for the debug build's index checks: the staging area, the
+  // exchange buffer (float4), the power tile (float2 and bytes), the output
+  const Cap in_cap = {(int)(lay.in_tile_bytes / sizeof(Raw)), prm.err};
+  const Cap x_cap = {kX2Lanes * GS4, prm.err}, p_cap = {(M + 1) * kX2Lanes, prm.err};
+  const int pw_off = 2 * (g & 7) + (g >> 3);
+  const long long out_total = prm.B * (long long)prm.n_mels * prm.n_frames;
 
   for (int k = 0;; ++k) {
     const long long tile = x2_tile(grp, k);
@@ -483,7 +515,7 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
     phase ^= 1u;
 
     cx2 z[Q];
-    pass1_load_x2<P, Q, HOP, Raw>(fbase, fbase_o, st.S, s_p1, role, z);
+    pass1_load_x2<P, Q, HOP, Raw>(fbase, fbase_o, st.S, s_p1, role, z, s_in, in_cap);
     dft<Q>(z);
 #pragma unroll
     for (int k2 = 1; k2 < Q; ++k2) {
@@ -498,13 +530,15 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
 #pragma unroll
     for (int k2 = 0; k2 < Q; ++k2) {
       float2* dst = reinterpret_cast<float2*>(xq_row + k2 * P + role);
-      dst[0] = z[k2].re;
-      dst[1] = z[k2].im;
+      if (FM_IN(g * GS4 + k2 * P + role < x_cap.n, prm.err)) {
+        dst[0] = z[k2].re;
+        dst[1] = z[k2].im;
+      }
     }
     group_sync(bar_id, THREADS);
 
     cx2 za[P], zb[P];
-    pass2_x2<P, Q>(xq_row, role, za, zb);
+    pass2_x2<P, Q>(xq_row, role, za, zb, g * GS4, x_cap);
     group_sync(bar_id, THREADS);  // exchange reads done
     if (tid == 0) {
       fence_proxy_async();  // the group's generic accesses before the producer's TMA writes
@@ -512,9 +546,9 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
     }
     const bool merged = role < 2;  // the warp that holds role 0 (and role 1)
     switch (prm.power_mode) {
-      case 0: split_x2<N, P, Q, 0>(za, zb, pw_col, s_twf4, role, prm.power, merged); break;
-      case 1: split_x2<N, P, Q, 1>(za, zb, pw_col, s_twf4, role, prm.power, merged); break;
-      default: split_x2<N, P, Q, 2>(za, zb, pw_col, s_twf4, role, prm.power, merged); break;
+      case 0: split_x2<N, P, Q, 0>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
+      case 1: split_x2<N, P, Q, 1>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
+      default: split_x2<N, P, Q, 2>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
     }
     group_sync(bar_id, THREADS);
 
@@ -528,10 +562,10 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
     const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
     if (prm.out_dtype == FM_F32)
       mel_project_x2(s_pw, s_desc, s_w4, static_cast<float*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
-                     s_end, lane);
+                     s_end, lane, p_cap.n * (int)sizeof(float2), prm.x2_slots, out_total - obase, prm.err);
     else
       mel_project_x2(s_pw, s_desc, s_w4, static_cast<__half*>(prm.out) + obase, n_valid, prm.n_frames, s_begin,
-                     s_end, lane);
+                     s_end, lane, p_cap.n * (int)sizeof(float2), prm.x2_slots, out_total - obase, prm.err);
   }
 }
 
