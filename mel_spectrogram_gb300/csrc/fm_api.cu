@@ -6,6 +6,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -16,6 +17,7 @@
 #include "fm_host.h"
 #include "fm_internal.h"
 #include "fm_kernel_big.cuh"
+#include "fm_kernel_c2c.cuh"
 #include "fm_mel.h"
 
 namespace fm {
@@ -23,6 +25,7 @@ extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant
     kVariant1024, kVariant2048, kVariant4096, kVariant8192, kVariant16384;
 extern const Variant kVariant64odd, kVariant128odd, kVariant256odd, kVariant400odd, kVariant512odd,
     kVariant1024odd, kVariant2048odd;
+extern const Variant kVariant400c2c;
 
 // The kernel for (n_fft, hop): a build for exactly this hop if there is one,
 // else the one for its parity (even hops stage and read aligned sample pairs,
@@ -34,6 +37,12 @@ const Variant* find_variant(int n_fft, int hop) {
                                  &kVariant128odd,  &kVariant256odd,  &kVariant400odd,  &kVariant512odd,
                                  &kVariant1024odd, &kVariant2048odd};
   const bool even = hop % 2 == 0;
+  // diagnostic A/B switch: the paired-frame complex transform at n_fft 400
+  // (even hops) instead of the two-frame packed kernel
+  if (n_fft == 400 && even) {
+    const char* k = std::getenv("FM_MEL_N400_KERNEL");
+    if (k != nullptr && std::strcmp(k, "c2c") == 0) return &kVariant400c2c;
+  }
   for (const Variant* v : all) {
     if (v->n_fft != n_fft) continue;
     if (v->hop > 0 ? v->hop == hop : (v->hop == kAnyHop || (v->hop == kEvenHops) == even)) return v;
@@ -77,6 +86,7 @@ struct fm_plan {
   mutable HostPipe pipe;  // streams and events of fm_mel_forward_host
   int x2_slots;         // its mel chunk slots
   int big_span;         // large-transform kernel: samples staged per tile (0: loads from global memory)
+  float2* c2c;          // paired-frame kernel: its pass-1 table, then W_400^j (inside dmem)
 };
 
 namespace {
@@ -317,6 +327,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   size_t smem_total =
       var->kind == 1   ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize, fm::kX2Groups).total
       : var->kind == 2 ? fm::big_layout(n_fft, n_mels, nnz).st
+      : var->kind == 3 ? fm::smem_layout_c2c(hop, n_mels, nnz, in_esize).total
                        : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
   if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_slots > fm::kX2MaxSlots ||
                          x2_warps > fm::kX2MaxWarps))
@@ -382,7 +393,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   const int S = var->kind == 1 ? fm::in_row_stride_x2(hop, in_esize) : fm::in_row_stride(hop);
   const float in_scale = in_dtype == FM_I16 ? 1.0f / 32768.0f : 1.0f;  // exact power of two
   std::vector<float4> p1(M);
-  for (int pp = 0; pp < var->P; ++pp)
+  for (int pp = 0; pp < var->P && var->kind != 3; ++pp)  // the paired-frame kernel has its own table
     for (int q = 0; q < var->Q; ++q) {
       const int j = 2 * (pp + var->P * q);
       const int off = (j / hop) * S + (j % hop);
@@ -410,6 +421,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   const size_t o_x2 = o;   o = fm::align16(o + (var->kind == 1 ? sizeof(fm::X2Tables) : 0));
   const size_t o_err = o;  o = fm::align16(o + sizeof(unsigned) * 4);
   const size_t o_win = o;  o = fm::align16(o + sizeof(float) * (var->kind == 2 ? n_fft : 0));
+  const size_t o_c2c = o;  o = fm::align16(o + sizeof(float2) * (var->kind == 3 ? 2 * fm::kC2cN : 0));
   std::vector<unsigned char> blob(o, 0);
   if (var->kind == 1) {
     fm::X2Tables* t = reinterpret_cast<fm::X2Tables*>(blob.data() + o_x2);
@@ -427,6 +439,22 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   std::memcpy(blob.data() + o_twf, twf.data(), sizeof(float2) * (M + 1));
   std::memcpy(blob.data() + o_mel, mel.data(), sizeof(int4) * n_mels);
   if (nnz > 0) std::memcpy(blob.data() + o_mw, mw.data(), sizeof(float) * nnz);
+  if (var->kind == 3) {
+    // paired-frame kernel: per (role p, step q) the window at n = p + P q
+    // (with the split's 1/2 and the int16 scale) and the tile offset of
+    // sample n (rows of hop samples, stride in_row_stride); then W_N^j, j < N
+    float2* tab = reinterpret_cast<float2*>(blob.data() + o_c2c);
+    for (int pp = 0; pp < fm::kC2cP; ++pp)
+      for (int q = 0; q < fm::kC2cQ; ++q) {
+        const int n = pp + fm::kC2cP * q;
+        const int off = (n / hop) * S + (n % hop);
+        tab[pp * fm::kC2cQ + q].x = win[n] * in_scale;
+        std::memcpy(&tab[pp * fm::kC2cQ + q].y, &off, sizeof(int));
+      }
+    std::vector<float2> tw400;
+    fm::build_twiddles(fm::kC2cN, fm::kC2cN, tw400);
+    std::memcpy(tab + fm::kC2cN, tw400.data(), sizeof(float2) * fm::kC2cN);
+  }
   if (var->kind == 2) {  // the window with the int16 scale, for the large-transform kernel
     float* wd = reinterpret_cast<float*>(blob.data() + o_win);
     for (int j = 0; j < n_fft; ++j) wd[j] = win[j] * in_scale;
@@ -453,6 +481,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   p->err = reinterpret_cast<unsigned*>(base + o_err);
   p->win = reinterpret_cast<float*>(base + o_win);
   p->x2 = var->kind == 1 ? reinterpret_cast<fm::X2Tables*>(base + o_x2) : nullptr;
+  p->c2c = reinterpret_cast<float2*>(base + o_c2c);
   *out = p;
   return FM_OK;
 }
@@ -529,6 +558,8 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.err = plan->err;
   prm.win = plan->win;
   prm.big_span = plan->big_span;
+  prm.c2c_tab = plan->c2c;
+  prm.c2c_tw = plan->c2c + fm::kC2cN;
 
   const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
   prm.x2 = plan->x2;

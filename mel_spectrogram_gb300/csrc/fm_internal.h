@@ -64,6 +64,8 @@ struct KernelParams {
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
   const float* win;       // the n_fft-point window (large-transform kernel only)
   int big_span;           // large-transform kernel: samples staged per tile in shared memory (0: none)
+  const float2* c2c_tab;  // paired-frame kernel: (window, tile offset) per role and step
+  const float2* c2c_tw;   // paired-frame kernel: W_400^j, j < 400
   // Packed kernel: when tmap_ok, every signal is described to the TMA unit as
   // rows of one staged line (line * in_bytes / 8 elements of 8 bytes) that
   // start at sample tmap_off + y * line, tmap_rows rows per signal, and the
@@ -114,7 +116,7 @@ __host__ __device__ inline SmemLayout smem_layout(int n_fft, int hop, int n_mels
 constexpr int kX2MaxM = 200;
 constexpr int kX2MaxMels = 256;
 constexpr int kX2MaxWarps = 16;
-constexpr int kX2Unroll = 4;    // chunks per unrolled mel iteration
+constexpr int kX2Unroll = 2;    // chunks per unrolled mel iteration
 constexpr int kX2Groups = 3;    // independent tile groups per CTA (one CTA per SM)
 constexpr int kX2ProducerWarps = 1;  // the warp that stages every group's tiles
 constexpr int kX2MaxSlots = 1024;  // mel chunk slots (4 chunks each) over all warps
@@ -212,7 +214,8 @@ struct Variant {
   int frames_per_tile;  // G: frames per tile = lanes per role
   int threads;          // P * G
   int in_buffers;       // 2: the next tile's input lands while this one computes
-  int kind;             // 0: one frame per thread; 1: two frames per thread (packed); 2: shared-memory passes
+  int kind;             // 0: one frame per thread; 1: two frames per thread (packed); 2: shared-memory passes;
+                        // 3: one complex transform per frame pair
   const void* fn;       // __global__ void(KernelParams)
   int hop;              // > 0: compiled for this hop only; else kEvenHops, kOddHops or kAnyHop
 };
