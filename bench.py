@@ -31,6 +31,7 @@ from mel_spectrogram_gb300.workloads import EXTRA, ORDER, WORKLOADS, make_input 
 
 BUFFER_SETS = 16
 HOST_SLACK_CYCLES = 200_000  # ~0.1 ms of device-side wait ahead of a timed region
+SINGLE_GRAPH_MAX = 512  # up to this many timed steps go into one captured graph
 L2_BYTES = 129 * 1024 * 1024
 def kernel_sha() -> str:
     """Fingerprint of the device code (every kernel source and header)."""
@@ -67,6 +68,20 @@ def recorded_traffic(workload: str):
         return None  # the kernel changed since the counters were taken
     v = d.get("bytes_per_launch", {}).get(workload)
     return float(v) if v is not None else None
+
+
+def recorded_l2_write_bytes(workload: str):
+    """L2 write sectors x 32 B per launch (the output side, which DRAM shows
+    only later as write-back), from the same record, if still current."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_sha") != kernel_sha():
+        return None
+    v = d.get("l2_write_sectors", {}).get(workload)
+    return 32.0 * v if v is not None else None
 
 
 def recorded_fma_pipe(workload: str):
@@ -191,7 +206,8 @@ class WorkloadRun:
                                self.s.cuda_stream)
 
     def graph(self, n, same_set=False):
-        """A CUDA graph of n launches over sets 0..n-1 (or n launches on set 0)."""
+        """A CUDA graph of n launches rotating over the buffer sets (i mod 16),
+        or of n launches on set 0."""
         import torch
 
         key = (n, same_set)
@@ -199,7 +215,7 @@ class WorkloadRun:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=self.s):
                 for i in range(n):
-                    self.launch(0 if same_set else i)
+                    self.launch(0 if same_set else i % BUFFER_SETS)
             with torch.cuda.stream(self.s):
                 g.replay()  # upload
             self.s.synchronize()
@@ -214,14 +230,22 @@ class WorkloadRun:
                 self.launch(i % BUFFER_SETS)
         self.s.synchronize()
 
+    def steps_graphs(self, K):
+        """The graphs that replay exactly K launches: one graph of K launches
+        when K is at most SINGLE_GRAPH_MAX (no gap between graph launches in
+        the timed region), else graphs of 16 launches and one of the rest."""
+        if K <= SINGLE_GRAPH_MAX:
+            return [self.graph(K)]
+        full, rest = divmod(K, BUFFER_SETS)
+        return [self.graph(BUFFER_SETS)] * full + ([self.graph(rest)] if rest else [])
+
     def timed_steps_ms(self, K):
         """Device time of exactly K launches replayed from graphs over the
         rotating sets. A device-side wait queued ahead of the start event keeps
         the host's graph submission out of the timed region."""
         import torch
 
-        full, rest = divmod(K, BUFFER_SETS)
-        gs = [self.graph(BUFFER_SETS)] * full + ([self.graph(rest)] if rest else [])
+        gs = self.steps_graphs(K)
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(self.s):
             torch.cuda._sleep(HOST_SLACK_CYCLES)
@@ -281,6 +305,7 @@ class WorkloadRun:
                 "peak_source": f"{pk['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                 "algorithmic_bytes_per_launch": in_b + out_b,
                 "traffic": recorded_traffic(w.name),
+                "l2_write_bytes": recorded_l2_write_bytes(w.name),
             },
             "fp32": {"achieved_tflops": flops / step_s / 1e12, "peak_tflops": fp32_peak,
                      "frac": flops / step_s / 1e12 / fp32_peak,
@@ -313,9 +338,7 @@ def run_gpu_arm(args) -> dict | None:
     run = WorkloadRun(fb, w, s)
     K, W = args.steps, args.warmup
     run.warm(W)
-    run.graph(BUFFER_SETS)
-    if K % BUFFER_SETS:
-        run.graph(K % BUFFER_SETS)
+    run.steps_graphs(K)  # captured and uploaded before the timed region
 
     with ClockSampler(local) as clk:
         if world > 1:
@@ -380,9 +403,7 @@ def run_gpu_arm(args) -> dict | None:
             r2 = WorkloadRun(fb, ow, s)
             K2 = min(K, args.other_steps)
             r2.warm(W)
-            r2.graph(BUFFER_SETS)
-            if K2 % BUFFER_SETS:
-                r2.graph(K2 % BUFFER_SETS)
+            r2.steps_graphs(K2)
             with ClockSampler(local) as c2:
                 torch.cuda.synchronize()
                 ta = time.time()
@@ -432,8 +453,10 @@ def run_gpu_arm(args) -> dict | None:
             "in_dtype": w.in_dtype, "out_dtype": w.out_dtype,
             "l2": f"{BUFFER_SETS} rotating input/output sets, "
                   f"{BUFFER_SETS * (in_b + out_b) / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB L2",
-            "launch": f"CUDA graphs of {BUFFER_SETS} fm_mel_forward launches, replayed; a device-side wait "
-                      "queued ahead of the start event keeps host submission out of the timed region",
+            "launch": (f"one CUDA graph of the {K} fm_mel_forward launches" if K <= SINGLE_GRAPH_MAX else
+                       f"CUDA graphs of {BUFFER_SETS} fm_mel_forward launches, replayed") +
+                      " over the rotating sets; a device-side wait queued ahead of the start event keeps host "
+                      "submission out of the timed region",
             "grid": min(info["grid_limit"], w.B * -(-nf // info["frames_per_tile"])),
             "block": info["threads_per_block"], "smem_bytes": info["smem_bytes"],
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
