@@ -381,11 +381,35 @@ def run_gpu_arm(args) -> dict | None:
     if world > 1:
         dist.barrier()
     e0.record(s)
+    h0 = time.perf_counter()
     for i in range(Ke):
         e2e_step(i % BUFFER_SETS)
+    enqueue_us = (time.perf_counter() - h0) * 1e6 / Ke  # host time to queue one step
     e1.record(s)
     s.synchronize()
     e_ms = e0.elapsed_time(e1)
+    # the same host-buffer call captured once into a CUDA graph and replayed
+    # (uploads, kernels and downloads as the call queued them): the device-side
+    # pipeline without the host's per-call queueing cost; reported beside e2e
+    ge_us = None
+    try:
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ge, stream=s):
+            e2e_step(0)
+        with torch.cuda.stream(s):
+            ge.replay()
+        s.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(HOST_SLACK_CYCLES)
+            g0.record(s)
+            for _ in range(Ke):
+                ge.replay()
+            g1.record(s)
+        s.synchronize()
+        ge_us = g0.elapsed_time(g1) * 1e3 / Ke
+    except RuntimeError:
+        ge_us = None
     if world > 1:
         t = torch.tensor([e_ms], device="cuda", dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -468,7 +492,11 @@ def run_gpu_arm(args) -> dict | None:
         "e2e": {"value": world * frames_step * Ke / (e_ms / 1e3), "unit": "frames/s",
                 "h2d_bytes_per_step": in_b, "d2h_bytes_per_step": out_b, "steps": Ke,
                 "api": "fm_mel_forward_host (pinned host buffers; per step the upload, kernel and download "
-                       "of up to four signal chunks, overlapped on plan-owned streams)"},
+                       "of up to four signal chunks, overlapped on plan-owned streams)",
+                "us_per_step": e_ms * 1e3 / Ke, "host_enqueue_us_per_step": enqueue_us,
+                "graph_replay_us_per_step": ge_us,
+                "graph_note": "the same call captured once into a CUDA graph and replayed (copies in the region); "
+                              "not the reported value"},
         "repeats": {"us_per_step": [round(v, 3) for v in repeat_us], "median_us": statistics.median(repeat_us),
                     "launches_each": reps * BUFFER_SETS,
                     "note": "cold L2 (16 rotating sets), timed after the main region"},
