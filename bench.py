@@ -1,6 +1,6 @@
 """Benchmark of the fused mel-spectrogram kernel on GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference] [--sweep]
 
 A step is one pass of the whole path (pad, frame, window, real DFT, |X|^p,
 mel projection) over one batch of the workload: one fm_mel_forward launch.
@@ -317,6 +317,54 @@ class WorkloadRun:
         self.fb.fm_plan_destroy(self.plan)
 
 
+def sweep_workloads():
+    """The flashmel README's size sweep ("Performance": hop = n_fft/4, 128 mels,
+    B=32, T=160000), one workload per supported n_fft, f32 in and out."""
+    from mel_spectrogram_gb300.workloads import Workload
+
+    sizes = [64, 128, 256, 400, 512, 1024, 2048, 4096, 8192, 16384]
+    return [Workload(f"sweep{n}", 32, 160000, "f32", "f32", 16000, n, n // 4, n, 128, 0.0, 8000.0, 2.0, "htk",
+                     None, "normal", 100 + i) for i, n in enumerate(sizes)]
+
+
+def run_sweep(args) -> dict:
+    """Time the size sweep on one GPU; one JSON line with a row per size."""
+    import torch
+
+    torch.cuda.set_device(0)
+    from mel_spectrogram_gb300.build import build
+
+    build()
+    from mel_spectrogram_gb300 import _binding as fb
+
+    s = torch.cuda.Stream()
+    props = torch.cuda.get_device_properties(0)
+    rows = {}
+    for w in sweep_workloads():
+        r = WorkloadRun(fb, w, s)
+        K = min(args.steps, args.other_steps)
+        r.warm(args.warmup)
+        r.steps_graphs(K)
+        with ClockSampler(0) as ck:
+            torch.cuda.synchronize()
+            ta = time.time()
+            ms = r.timed_steps_ms(K)
+            torch.cuda.synchronize()
+            tb = time.time()
+        clk = ck.summary(ta, tb)
+        assert fb.fm_plan_poll_error(r.plan) == fb.FM_OK
+        fig = r.figures(ms / 1e3 / K, clk["sm_mhz"] or peaks()["sm_max_mhz"], props)
+        rows[w.name] = {"n_fft": w.n_fft, "hop": w.hop, "us_per_step": ms * 1e3 / K,
+                        "hbm_frac": fig["roofline"]["frac"], "hbm_gbs": fig["hbm_gbs"],
+                        "fp32_frac": fig["fp32"]["frac"], "frames_per_s": fig["frames_per_s"],
+                        "threads_per_block": r.info["threads_per_block"], "frames_per_tile": r.info["frames_per_tile"],
+                        "blocks_per_sm": r.info["blocks_per_sm"], "clocks": clk}
+        r.close()
+    return {"sweep": "flashmel README size sweep: hop = n_fft/4, 128 mels, B=32 x T=160000 f32, sr 16000, "
+                     "HTK, power 2, f32 out; kernel only, 16 rotating input/output sets",
+            "steps": min(args.steps, args.other_steps), "rows": rows}
+
+
 def run_gpu_arm(args) -> dict | None:
     import torch
     import torch.distributed as dist
@@ -601,11 +649,16 @@ def main() -> int:
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", action="store_true", help="time the chosen workload only")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every n_fft on the pages' sweep configuration instead (one JSON line)")
     ap.add_argument("--other-steps", type=int, default=2000,
                     help="timed steps of each of the other workloads (at most --steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.sweep:
+        print(json.dumps(run_sweep(args)), flush=True)
+        return 0
     line = run_reference_arm(args) if args.impl == "reference" else run_gpu_arm(args)
     if line is not None:
         print(json.dumps(line), flush=True)
