@@ -1,6 +1,6 @@
-// n_fft = 64 (M = 4 x 8) and 256 (M = 8 x 16): two frames per thread, packed;
-// n_fft = 128 (M = 8 x 8): one frame per thread
+// n_fft = 64 (M = 4 x 8), 128 (M = 8 x 8) and 256 (M = 8 x 16): two frames
+// per thread, packed
 #include "fm_kernel_x2.cuh"
 FM_DEFINE_VARIANT_X2(kVariant64, 64, 4, 8, 0)
-FM_DEFINE_VARIANT(kVariant128, 128, 8, 8, 32, 2)
+FM_DEFINE_VARIANT_X2(kVariant128, 128, 8, 8, 0)
 FM_DEFINE_VARIANT_X2(kVariant256, 256, 8, 16, 0)

@@ -1,5 +1,5 @@
 // Two-frames-per-thread variant of the fused mel kernel (sm_103a), for the
-// splits with Q = 2P (n_fft = 400, 256, 64).
+// splits with Q = 2P (n_fft = 400, 256, 64) and Q = P (n_fft = 128).
 //
 // Same path and same four-step real FFT as fm_kernel.cuh, but a tile holds 32
 // frames and thread (role, g), g < 16, carries frames g and g + 16 through
@@ -187,6 +187,53 @@ __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], f
       split_pair_x2<MODE>(u, v, s_twf4[k], pw, lo, hi);
       put(pw_col, poff, k * kX2Lanes, lo, p_cap);
       put(pw_col, poff, (M - k) * kX2Lanes, hi, p_cap);
+    }
+  }
+}
+
+// Pass 2 and split when Q = P (n_fft 128): role t does the P-point DFT over p
+// for k2 = t, Z[t + Q k1] goes back through the exchange buffer in natural
+// order, and role t then splits the pairs (k, M - k), k = t + P i <= M/2
+// (k = 0 gives X[0] and X[M]). The power values stay in registers until every
+// thread has read its Z, since the power tile and the next staged tile
+// overwrite the buffer; `freed` then releases the staging area.
+template <int N, int P, int MODE, typename Freed>
+__device__ __forceinline__ void pass2_split_exchange_x2(float4* xq_row, float2* pw_col, const float4* __restrict__ s_twf4,
+                                                        int t, float pw, int xoff, Cap x_cap, int poff, Cap p_cap,
+                                                        int bar_id, int threads, Freed freed) {
+  constexpr int M = N / 2, Q = P;
+  constexpr int PER = (M / 2) / P + 1;
+  cx2 y[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const float4 v = get(xq_row, xoff, t * P + p, x_cap);
+    y[p] = {make_float2(v.x, v.y), make_float2(v.z, v.w)};
+  }
+  dft<P>(y);
+  group_sync(bar_id, threads);  // every pass-1 value read before Z overwrites the rows
+#pragma unroll
+  for (int k1 = 0; k1 < P; ++k1)
+    put(xq_row, xoff, t + Q * k1, make_float4(y[k1].re.x, y[k1].re.y, y[k1].im.x, y[k1].im.y), x_cap);
+  group_sync(bar_id, threads);
+  float2 lo[PER], hi[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int k = t + P * i;
+    lo[i] = hi[i] = make_float2(0.0f, 0.0f);
+    if (k <= M / 2) {
+      const float4 a = get(xq_row, xoff, k, x_cap), b = get(xq_row, xoff, (M - k) % M, x_cap);
+      split_pair_x2<MODE>({make_float2(a.x, a.y), make_float2(a.z, a.w)}, {make_float2(b.x, b.y), make_float2(b.z, b.w)},
+                          s_twf4[k], pw, lo[i], hi[i]);
+    }
+  }
+  group_sync(bar_id, threads);  // every Z read: the power tile and the next staged tile may land
+  freed();
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int k = t + P * i;
+    if (k <= M / 2) {
+      put(pw_col, poff, k * kX2Lanes, lo[i], p_cap);
+      put(pw_col, poff, (M - k) * kX2Lanes, hi[i], p_cap);
     }
   }
 }
@@ -537,18 +584,40 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
     }
     group_sync(bar_id, THREADS);
 
-    cx2 za[P], zb[P];
-    pass2_x2<P, Q>(xq_row, role, za, zb, g * GS4, x_cap);
-    group_sync(bar_id, THREADS);  // exchange reads done
-    if (tid == 0) {
-      fence_proxy_async();  // the group's generic accesses before the producer's TMA writes
-      mbar_arrive(empty);   // the staging area (upper half) is free for the next tile
-    }
-    const bool merged = role < 2;  // the warp that holds role 0 (and role 1)
-    switch (prm.power_mode) {
-      case 0: split_x2<N, P, Q, 0>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
-      case 1: split_x2<N, P, Q, 1>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
-      default: split_x2<N, P, Q, 2>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
+    // the staging area (upper half) is free for the next tile once the
+    // exchange buffer has been read for the last time
+    const auto freed = [&] {
+      if (tid == 0) {
+        fence_proxy_async();  // the group's generic accesses before the producer's TMA writes
+        mbar_arrive(empty);
+      }
+    };
+    if constexpr (Q == 2 * P) {
+      cx2 za[P], zb[P];
+      pass2_x2<P, Q>(xq_row, role, za, zb, g * GS4, x_cap);
+      group_sync(bar_id, THREADS);  // exchange reads done
+      freed();
+      const bool merged = role < 2;  // the warp that holds role 0 (and role 1)
+      switch (prm.power_mode) {
+        case 0: split_x2<N, P, Q, 0>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
+        case 1: split_x2<N, P, Q, 1>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
+        default: split_x2<N, P, Q, 2>(za, zb, pw_col, s_twf4, role, prm.power, merged, pw_off, p_cap); break;
+      }
+    } else {
+      switch (prm.power_mode) {
+        case 0:
+          pass2_split_exchange_x2<N, P, 0>(xq_row, pw_col, s_twf4, role, prm.power, g * GS4, x_cap, pw_off, p_cap,
+                                           bar_id, THREADS, freed);
+          break;
+        case 1:
+          pass2_split_exchange_x2<N, P, 1>(xq_row, pw_col, s_twf4, role, prm.power, g * GS4, x_cap, pw_off, p_cap,
+                                           bar_id, THREADS, freed);
+          break;
+        default:
+          pass2_split_exchange_x2<N, P, 2>(xq_row, pw_col, s_twf4, role, prm.power, g * GS4, x_cap, pw_off, p_cap,
+                                           bar_id, THREADS, freed);
+          break;
+      }
     }
     group_sync(bar_id, THREADS);
 
@@ -578,7 +647,7 @@ __global__ void __launch_bounds__(kX2Groups* P* kX2Lanes + 32 * kX2ProducerWarps
   constexpr int M = N / 2;
   constexpr int GROUP = P * kX2Lanes;
   constexpr int CONSUMERS = kX2Groups * GROUP;
-  static_assert(P * Q == M && Q == 2 * P && M <= kX2MaxM, "x2 kernel needs Q = 2P and M <= 200");
+  static_assert(P * Q == M && (Q == 2 * P || Q == P) && M <= kX2MaxM, "x2 kernel needs Q = 2P or P and M <= 200");
   static_assert(GROUP % 32 == 0, "a group must be whole warps");
   static_assert(kX2ProducerWarps == 1, "one producer warp");
   extern __shared__ __align__(128) unsigned char smem[];
