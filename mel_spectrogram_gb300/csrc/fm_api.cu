@@ -21,29 +21,37 @@
 #include "fm_mel.h"
 
 namespace fm {
-extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant400h160, kVariant512,
+extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant400h160, kVariant512x2, kVariant512,
     kVariant1024, kVariant2048, kVariant4096, kVariant8192, kVariant16384;
+extern const Variant kVariant64one, kVariant128one, kVariant256one, kVariant400one;
 extern const Variant kVariant64odd, kVariant128odd, kVariant256odd, kVariant400odd, kVariant512odd,
     kVariant1024odd, kVariant2048odd;
 extern const Variant kVariant400c2c;
 
-// The kernel for (n_fft, hop): a build for exactly this hop if there is one,
-// else the one for its parity (even hops stage and read aligned sample pairs,
-// odd hops take the generic kernel's contiguous staging), else one for any hop.
-const Variant* find_variant(int n_fft, int hop) {
-  static const Variant* all[] = {&kVariant400h160, &kVariant64,      &kVariant128,     &kVariant256,
-                                 &kVariant400,     &kVariant512,     &kVariant1024,    &kVariant2048,
-                                 &kVariant4096,    &kVariant8192,    &kVariant16384,   &kVariant64odd,
-                                 &kVariant128odd,  &kVariant256odd,  &kVariant400odd,  &kVariant512odd,
-                                 &kVariant1024odd, &kVariant2048odd};
+// The kernels for (n_fft, hop), in order: a build for exactly this hop if
+// there is one, then those for its parity (even hops stage and read aligned
+// sample pairs, the packed two-frame kernel ahead of the one-frame kernel;
+// odd hops take the generic kernel's contiguous staging), then one for any hop.
+const Variant* find_variant(int n_fft, int hop, const Variant* after) {
+  static const Variant* all[] = {&kVariant400h160, &kVariant64,      &kVariant64one,   &kVariant128,
+                                 &kVariant128one,  &kVariant256,     &kVariant256one,  &kVariant400,
+                                 &kVariant400one,  &kVariant512x2,   &kVariant512,     &kVariant1024,
+                                 &kVariant2048,    &kVariant4096,    &kVariant8192,    &kVariant16384,
+                                 &kVariant64odd,   &kVariant128odd,  &kVariant256odd,  &kVariant400odd,
+                                 &kVariant512odd,  &kVariant1024odd, &kVariant2048odd};
   const bool even = hop % 2 == 0;
   // diagnostic A/B switch: the paired-frame complex transform at n_fft 400
   // (even hops) instead of the two-frame packed kernel
-  if (n_fft == 400 && even) {
+  if (after == nullptr && n_fft == 400 && even) {
     const char* k = std::getenv("FM_MEL_N400_KERNEL");
     if (k != nullptr && std::strcmp(k, "c2c") == 0) return &kVariant400c2c;
   }
+  bool skip = after != nullptr && after != &kVariant400c2c;  // up to and including `after`
   for (const Variant* v : all) {
+    if (skip) {
+      skip = v != after;
+      continue;
+    }
     if (v->n_fft != n_fft) continue;
     if (v->hop > 0 ? v->hop == hop : (v->hop == kAnyHop || (v->hop == kEvenHops) == even)) return v;
   }
@@ -295,8 +303,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   fm_status st = fm::check_filter_args(sr, n_fft, n_mels, f_min, &f_max, mel_scale, norm);
   if (st != FM_OK) return st;
   if (!fm::is_supported_nfft(n_fft) || n_mels > 256) return FM_ERR_UNSUPPORTED;
-  const fm::Variant* var = fm::find_variant(n_fft, hop);
-  if (var == nullptr) return FM_ERR_UNSUPPORTED;
+  if (fm::find_variant(n_fft, hop) == nullptr) return FM_ERR_UNSUPPORTED;
 
   // host tables (double precision, rounded to float)
   std::vector<int> ms, ml, mo;
@@ -313,32 +320,45 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
     return FM_ERR_OOM;
   }
   const int nnz = (int)mw.size();
-  X2Schedule x2s;
-  // warps per tile group of the packed kernel (its CTA adds the producer warp)
-  const int x2_warps = (var->threads / 32 - fm::kX2ProducerWarps) / fm::kX2Groups;
-  if (var->kind == 1) x2s = build_x2_schedule(n_fft / 2, n_mels, x2_warps, ms, ml, mo, mw);
-  const int x2_slots = var->kind == 1 ? x2s.warp_begin.back() : 0;
 
   int dev = 0;
   cudaDeviceProp prop;
   if (cudaGetDevice(&dev) != cudaSuccess) return FM_ERR_CUDA;
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return FM_ERR_CUDA;
   const int in_esize = in_dtype == FM_F32 ? 4 : 2;
-  size_t smem_total =
-      var->kind == 1   ? fm::smem_layout_x2(n_fft, hop, var->hop > 0 ? 2 : 1, x2_slots, in_esize, fm::kX2Groups).total
-      : var->kind == 2 ? fm::big_layout(n_fft, n_mels, nnz).st
-      : var->kind == 3 ? fm::smem_layout_c2c(hop, n_mels, nnz, in_esize).total
-                       : fm::smem_layout(n_fft, hop, n_mels, nnz, var->frames_per_tile, in_esize, var->in_buffers).total;
-  if (var->kind == 1 && (n_fft / 2 > fm::kX2MaxM || x2_slots > fm::kX2MaxSlots ||
-                         x2_warps > fm::kX2MaxWarps))
-    return FM_ERR_UNSUPPORTED;
-  // the kernel's static shared memory comes out of the same per-block limit
-  cudaFuncAttributes fattr;
-  if (cudaFuncGetAttributes(&fattr, var->fn) != cudaSuccess) return FM_ERR_CUDA;
-  const size_t dyn_max = prop.sharedMemPerBlockOptin > fattr.sharedSizeBytes
+  // the first kernel for (n_fft, hop) whose tables and shared memory fit
+  const fm::Variant* var = nullptr;
+  X2Schedule x2s;
+  int x2_slots = 0;
+  size_t smem_total = 0, dyn_max = 0;
+  for (const fm::Variant* v = fm::find_variant(n_fft, hop); v != nullptr && var == nullptr;
+       v = fm::find_variant(n_fft, hop, v)) {
+    // warps per tile group of the packed kernel (its CTA adds the producer warp)
+    const int x2_warps = v->kind == 1 ? (v->threads / 32 - fm::kX2ProducerWarps) / v->groups : 0;
+    X2Schedule sched;
+    if (v->kind == 1) sched = build_x2_schedule(n_fft / 2, n_mels, x2_warps, ms, ml, mo, mw);
+    const int slots = v->kind == 1 ? sched.warp_begin.back() : 0;
+    if (v->kind == 1 && (n_fft / 2 > fm::kX2MaxM || slots > fm::kX2MaxSlots || x2_warps > fm::kX2MaxWarps))
+      continue;
+    const size_t need =
+        v->kind == 1   ? fm::smem_layout_x2(n_fft, hop, v->hop > 0 ? 2 : 1, slots, in_esize, v->groups).total
+        : v->kind == 2 ? fm::big_layout(n_fft, n_mels, nnz).st
+        : v->kind == 3 ? fm::smem_layout_c2c(hop, n_mels, nnz, in_esize).total
+                       : fm::smem_layout(n_fft, hop, n_mels, nnz, v->frames_per_tile, in_esize, v->in_buffers).total;
+    // the kernel's static shared memory comes out of the same per-block limit
+    cudaFuncAttributes fattr;
+    if (cudaFuncGetAttributes(&fattr, v->fn) != cudaSuccess) return FM_ERR_CUDA;
+    const size_t avail = prop.sharedMemPerBlockOptin > fattr.sharedSizeBytes
                              ? prop.sharedMemPerBlockOptin - fattr.sharedSizeBytes
                              : 0;
-  if (smem_total > dyn_max) return FM_ERR_UNSUPPORTED;
+    if (need > avail) continue;
+    var = v;
+    x2s = std::move(sched);
+    x2_slots = slots;
+    smem_total = need;
+    dyn_max = avail;
+  }
+  if (var == nullptr) return FM_ERR_UNSUPPORTED;
   // large-transform kernel: a staging buffer for the next tile's samples, when
   // one tile's span fits beside the transform buffer
   int big_span = 0;
@@ -564,12 +584,12 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   const long long grid = prm.total_tiles < plan->grid_limit ? prm.total_tiles : plan->grid_limit;
   prm.x2 = plan->x2;
   // two-frames-per-thread kernel: move the signals' first and last tiles (the
-  // slow ones to stage) into the third group's first slots, when there are at
+  // slow ones to stage) into the last group's first slots, when there are at
   // most as many as CTAs and every slot they take holds an interior tile
   prm.perm_edges = 0;
   prm.perm_t0 = 0;
   if (v->kind == 1) {
-    const long long tps = prm.tiles_per_signal, n_edge = 2 * B, t0 = (long long)(fm::kX2Groups - 1) * grid;
+    const long long tps = prm.tiles_per_signal, n_edge = 2 * B, t0 = (long long)(v->groups - 1) * grid;
     if (tps >= 3 && n_edge <= grid && t0 + n_edge <= prm.total_tiles) {
       bool ok = true;
       for (long long i = 0; i < n_edge && ok; ++i) {

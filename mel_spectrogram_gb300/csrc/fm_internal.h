@@ -111,13 +111,12 @@ __host__ __device__ inline SmemLayout smem_layout(int n_fft, int hop, int n_mels
 }
 
 // Constant tables of the two-frames-per-thread kernel, in one device block
-// that each CTA copies into shared memory. Sized for n_fft <= 400 (M <= 200):
+// that each CTA copies into shared memory. Sized for n_fft <= 512 (M <= 256):
 // every bin lies in at most two triangles, so nnz <= 2 (M + 1).
-constexpr int kX2MaxM = 200;
+constexpr int kX2MaxM = 256;
 constexpr int kX2MaxMels = 256;
 constexpr int kX2MaxWarps = 16;
 constexpr int kX2Unroll = 2;    // chunks per unrolled mel iteration
-constexpr int kX2Groups = 3;    // independent tile groups per CTA (one CTA per SM)
 constexpr int kX2ProducerWarps = 1;  // the warp that stages every group's tiles
 constexpr int kX2MaxSlots = 1024;  // mel chunk slots (4 chunks each) over all warps
 struct X2Tables {
@@ -218,6 +217,7 @@ struct Variant {
                         // 3: one complex transform per frame pair
   const void* fn;       // __global__ void(KernelParams)
   int hop;              // > 0: compiled for this hop only; else kEvenHops, kOddHops or kAnyHop
+  int groups;           // kind 1: independent tile groups per CTA (one CTA per SM); else 0
 };
 
 // Variant::hop values other than a compiled-in hop
@@ -225,7 +225,9 @@ constexpr int kEvenHops = 0;   // any even hop (samples staged and read in align
 constexpr int kOddHops = -1;   // any odd hop (contiguous staging, pairs read as two samples)
 constexpr int kAnyHop = -2;    // any hop (the large-transform kernel reads single samples)
 
-// the kernel for (n_fft, hop): a hop-specialised build if there is one
-const Variant* find_variant(int n_fft, int hop);
+// The kernels for (n_fft, hop) in order of preference (a hop-specialised build
+// first): the first one, or with `after` the one that follows it; nullptr
+// when there is none left. The plan takes the first whose shared memory fits.
+const Variant* find_variant(int n_fft, int hop, const Variant* after = nullptr);
 
 }  // namespace fm

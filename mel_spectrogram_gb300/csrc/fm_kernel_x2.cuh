@@ -1,5 +1,5 @@
 // Two-frames-per-thread variant of the fused mel kernel (sm_103a), for the
-// splits with Q = 2P (n_fft = 400, 256, 64) and Q = P (n_fft = 128).
+// splits with Q = 2P (n_fft = 400, 256, 64) and Q = P (n_fft = 128, 512).
 //
 // Same path and same four-step real FFT as fm_kernel.cuh, but a tile holds 32
 // frames and thread (role, g), g < 16, carries frames g and g + 16 through
@@ -191,7 +191,7 @@ __device__ __forceinline__ void split_x2(const cx2 (&a)[P], const cx2 (&b)[P], f
   }
 }
 
-// Pass 2 and split when Q = P (n_fft 128): role t does the P-point DFT over p
+// Pass 2 and split when Q = P (n_fft 128, 512): role t does the P-point DFT over p
 // for k2 = t, Z[t + Q k1] goes back through the exchange buffer in natural
 // order, and role t then splits the pairs (k, M - k), k = t + P i <= M/2
 // (k = 0 gives X[0] and X[M]). The power values stay in registers until every
@@ -293,16 +293,17 @@ __device__ __forceinline__ void mel_project_x2(const unsigned char* s_pw, const 
   }
 }
 
-// Tile k of tile group g of this CTA: groups take the grid's tile slots in
-// turn, so group g runs tiles blockIdx.x + gridDim.x * (g + kX2Groups * k).
+// Tile k of tile group g of this CTA (GR groups): groups take the grid's tile
+// slots in turn, so group g runs tiles blockIdx.x + gridDim.x * (g + GR k).
+template <int GR>
 __device__ __forceinline__ long long x2_tile(int g, int k) {
-  return (long long)blockIdx.x + (long long)gridDim.x * (g + (long long)kX2Groups * k);
+  return (long long)blockIdx.x + (long long)gridDim.x * (g + (long long)GR * k);
 }
 
 // The tile that slot p processes. A signal's first and last tiles take
 // padding and are the slowest to stage; the host may swap them (perm_edges)
 // with interior tiles of the slots [perm_t0, perm_t0 + perm_edges), which it
-// sets to the third group's first tiles: that group has the fewest tiles, so
+// sets to the last group's first tiles: that group has the fewest tiles, so
 // a late start costs it nothing, and no later round then waits behind an
 // edge tile. Edge tile 2b is signal b's first, 2b + 1 its last.
 __device__ __forceinline__ long long x2_logical(const KernelParams& prm, const TileSplitter& split, long long p) {
@@ -375,7 +376,7 @@ __device__ __forceinline__ void stage_lines_reflect(const Raw* __restrict__ sig,
 // buffer); the warp serves whichever group is ready first. Waits are bounded:
 // if no group frees its area for ~2^22 polls the warp records
 // FM_ERR_KERNEL_TIMEOUT and stops staging (the waiting groups then time out).
-template <int N, int HOP, typename Raw>
+template <int N, int GR, int HOP, typename Raw>
 __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay,
                                            int lane) {
   const X2Staging<N, HOP, Raw> st(prm.hop);
@@ -385,7 +386,7 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
   const TileSplitter split(prm.tiles_per_signal);
   const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
   unsigned long long* full = reinterpret_cast<unsigned long long*>(smem + lay.bars);
-  unsigned long long* empty = full + kX2Groups;
+  unsigned long long* empty = full + GR;
   // The tensor map's rows are lines of L samples starting at signal index
   // tmap_off, and lead + tmap_off is a multiple of L, so tile tt's first line
   // is tensor row tt * kX2Frames / KH - y_lead.
@@ -466,14 +467,14 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     __syncwarp();  // every lane's pending arrival is registered before lane 0's
     if (lane == 0) mbar_arrive(full + g);
   };
-  int next_k[kX2Groups];
-  unsigned phase[kX2Groups];
+  int next_k[GR];
+  unsigned phase[GR];
 #pragma unroll
-  for (int g = 0; g < kX2Groups; ++g) {
+  for (int g = 0; g < GR; ++g) {
     phase[g] = 0u;
     next_k[g] = 0;
-    if (x2_tile(g, 0) < prm.total_tiles) {
-      stage(g, x2_logical(prm, split, x2_tile(g, 0)), 0);
+    if (x2_tile<GR>(g, 0) < prm.total_tiles) {
+      stage(g, x2_logical(prm, split, x2_tile<GR>(g, 0)), 0);
       next_k[g] = 1;
     }
   }
@@ -481,8 +482,8 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     int ready = -1;
     bool left = false;
 #pragma unroll
-    for (int g = 0; g < kX2Groups; ++g) {
-      if (x2_tile(g, next_k[g]) >= prm.total_tiles) continue;
+    for (int g = 0; g < GR; ++g) {
+      if (x2_tile<GR>(g, next_k[g]) >= prm.total_tiles) continue;
       left = true;
       if (ready < 0 && mbar_test_wait(empty + g, phase[g])) ready = g;
     }
@@ -497,7 +498,7 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
     }
     idle = 0;
     phase[ready] ^= 1u;
-    stage(ready, x2_logical(prm, split, x2_tile(ready, next_k[ready])), next_k[ready]);
+    stage(ready, x2_logical(prm, split, x2_tile<GR>(ready, next_k[ready])), next_k[ready]);
     ++next_k[ready];
   }
   cp_async_wait_all();  // no copy of this warp stays in flight past its exit
@@ -515,7 +516,7 @@ __device__ __forceinline__ void produce_x2(const KernelParams& prm, unsigned cha
 //   split and |X|^p; barrier; mel projection and stores.
 // A warp that finishes its mel work early runs the next tile's pass 1 while
 // the others finish theirs.
-template <int N, int P, int Q, int HOP, typename Raw>
+template <int N, int P, int Q, int GR, int HOP, typename Raw>
 __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned char* smem, const SmemLayoutX2& lay,
                                            int grp) {
   constexpr int M = N / 2;
@@ -530,7 +531,7 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
   float4* s_xq = reinterpret_cast<float4*>(s_x);
   const int bar_id = 1 + grp;
   unsigned long long* full = reinterpret_cast<unsigned long long*>(smem + lay.bars) + grp;
-  unsigned long long* empty = full + kX2Groups;
+  unsigned long long* empty = full + GR;
 
   const int tid = threadIdx.x - grp * THREADS, warp = tid >> 5, lane = tid & 31;
   const int g = tid % kX2Lanes, role = tid / kX2Lanes;
@@ -556,7 +557,7 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
   const long long out_total = prm.B * (long long)prm.n_mels * prm.n_frames;
 
   for (int k = 0;; ++k) {
-    const long long tile = x2_tile(grp, k);
+    const long long tile = x2_tile<GR>(grp, k);
     if (tile >= prm.total_tiles) break;
     const bool ok = mbar_wait_bounded(full, phase, prm.err);
     phase ^= 1u;
@@ -638,26 +639,30 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
   }
 }
 
-// One CTA per SM: kX2Groups tile groups of P x 16 threads, each running its
-// own tile loop on its own exchange buffer, and one producer warp that stages
-// all their tiles; the tables are shared.
-template <int N, int P, int Q, int HOP>
-__global__ void __launch_bounds__(kX2Groups* P* kX2Lanes + 32 * kX2ProducerWarps, 1)
+// One CTA per SM: GR tile groups of P x 16 threads, each running its own tile
+// loop on its own exchange buffer, and one producer warp that stages all their
+// tiles; the tables are shared.
+template <int N, int P, int Q, int GR, int HOP>
+__global__ void __launch_bounds__(GR* P* kX2Lanes + 32 * kX2ProducerWarps, 1)
     mel_kernel_x2(const __grid_constant__ KernelParams prm) {
   constexpr int M = N / 2;
   constexpr int GROUP = P * kX2Lanes;
-  constexpr int CONSUMERS = kX2Groups * GROUP;
-  static_assert(P * Q == M && (Q == 2 * P || Q == P) && M <= kX2MaxM, "x2 kernel needs Q = 2P or P and M <= 200");
+  constexpr int CONSUMERS = GR * GROUP;
+  static_assert(P * Q == M && (Q == 2 * P || Q == P) && M <= kX2MaxM, "x2 kernel needs Q = 2P or P and M <= 256");
+  static_assert(GR >= 1 && GR <= 14, "named barriers 1..GR + 1");
   static_assert(GROUP % 32 == 0, "a group must be whole warps");
   static_assert(kX2ProducerWarps == 1, "one producer warp");
-  extern __shared__ __align__(128) unsigned char smem[];
+  // (its own name: a translation unit that also holds the one-frame kernel
+  // declares that kernel's dynamic shared array with 16-byte alignment)
+  extern __shared__ __align__(128) unsigned char smem_x2[];
+  unsigned char* const smem = smem_x2;
   const int esize = prm.in_dtype == FM_F32 ? 4 : 2;
-  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, HOP > 0 ? 2 : 1, prm.x2_slots, esize, kX2Groups);
+  const SmemLayoutX2 lay = smem_layout_x2(N, prm.hop, HOP > 0 ? 2 : 1, prm.x2_slots, esize, GR);
   pdl_launch_dependents();
   const int tid = threadIdx.x;
   if (tid == CONSUMERS) {
     unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem + lay.bars);
-    for (int i = 0; i < 2 * kX2Groups; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < 2 * GR; ++i) mbar_init(bars + i, 1);
     fence_mbar_init();
   }
   // tables, fetched once per CTA by the consumer threads
@@ -672,28 +677,29 @@ __global__ void __launch_bounds__(kX2Groups* P* kX2Lanes + 32 * kX2ProducerWarps
   pdl_wait();       // caller buffers only after the previous kernel in the stream is done
   __syncthreads();  // the mbarriers exist before anyone uses them
   if (tid >= CONSUMERS) {
-    if (prm.in_dtype == FM_F32) produce_x2<N, HOP, float>(prm, smem, lay, tid & 31);
-    else if (prm.in_dtype == FM_I16) produce_x2<N, HOP, short>(prm, smem, lay, tid & 31);
-    else produce_x2<N, HOP, __half>(prm, smem, lay, tid & 31);
+    if (prm.in_dtype == FM_F32) produce_x2<N, GR, HOP, float>(prm, smem, lay, tid & 31);
+    else if (prm.in_dtype == FM_I16) produce_x2<N, GR, HOP, short>(prm, smem, lay, tid & 31);
+    else produce_x2<N, GR, HOP, __half>(prm, smem, lay, tid & 31);
     return;
   }
   cp_async_wait_all();
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + kX2Groups), "r"(CONSUMERS) : "memory");  // tables visible
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + GR), "r"(CONSUMERS) : "memory");  // tables visible
   // warp-uniform (a group is whole warps); reading it through a shuffle lets
   // the compiler keep the group's base addresses in uniform registers
   const int grp = __shfl_sync(0xffffffffu, tid / GROUP, 0);
-  if (prm.in_dtype == FM_F32) consume_x2<N, P, Q, HOP, float>(prm, smem, lay, grp);
-  else if (prm.in_dtype == FM_I16) consume_x2<N, P, Q, HOP, short>(prm, smem, lay, grp);
-  else consume_x2<N, P, Q, HOP, __half>(prm, smem, lay, grp);
+  if (prm.in_dtype == FM_F32) consume_x2<N, P, Q, GR, HOP, float>(prm, smem, lay, grp);
+  else if (prm.in_dtype == FM_I16) consume_x2<N, P, Q, GR, HOP, short>(prm, smem, lay, grp);
+  else consume_x2<N, P, Q, GR, HOP, __half>(prm, smem, lay, grp);
 }
 
 }  // namespace fm
 
 // Instantiate one two-frames-per-thread variant:
-// FM_DEFINE_VARIANT_X2(name, N, P, Q, HOP) with HOP = 0 for any even hop
-#define FM_DEFINE_VARIANT_X2(NAME, N, P, Q, HOP)                                                       \
-  namespace fm {                                                                                       \
-  template __global__ void mel_kernel_x2<N, P, Q, HOP>(const __grid_constant__ KernelParams);        \
-  extern const Variant NAME = {N,  P, Q, kX2Frames, kX2Groups * P * kX2Lanes + 32 * kX2ProducerWarps, \
-                               2,  1, (const void*)&mel_kernel_x2<N, P, Q, HOP>, HOP};                \
+// FM_DEFINE_VARIANT_X2(name, N, P, Q, GR, HOP), GR tile groups per CTA, HOP = 0
+// for any even hop
+#define FM_DEFINE_VARIANT_X2(NAME, N, P, Q, GR, HOP)                                                    \
+  namespace fm {                                                                                        \
+  template __global__ void mel_kernel_x2<N, P, Q, GR, HOP>(const __grid_constant__ KernelParams);     \
+  extern const Variant NAME = {N, P, Q, kX2Frames, GR * P * kX2Lanes + 32 * kX2ProducerWarps,          \
+                               2, 1, (const void*)&mel_kernel_x2<N, P, Q, GR, HOP>, HOP, GR};           \
   }

@@ -1,0 +1,62 @@
+"""Even hops on both sides of the packed kernel's shared-memory limit.
+
+The packed two-frame kernel (n_fft 64 to 512) keeps one exchange buffer and
+one staged tile per tile group. Once a long hop's staged tile no longer fits,
+the plan takes the one-frame kernel of the same size instead; torchaudio's
+default hop at n_fft 400 (win_length // 2 = 200) is such a hop. Every case
+checks every output element against the float64 oracle, and each size is
+shown to run both kernels over its hop list (their CTA sizes differ)."""
+from __future__ import annotations
+
+import pytest
+
+from mel_spectrogram_gb300 import _binding as fb
+from mel_spectrogram_gb300.workloads import Workload, make_input
+from tests.gpu_util import check_close, oracle_for, plan_for, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mel_spectrogram_gb300.build import build
+
+    build()
+
+
+# per size: short hops, n_fft/4, n_fft/2, n_fft, and hops past the packed
+# kernel's staging room that the one-frame kernel still takes
+HOPS = {
+    64: [2, 16, 32, 64, 600, 800],
+    128: [2, 32, 64, 128, 500, 800],
+    256: [2, 64, 128, 256, 500, 700],
+    400: [2, 100, 160, 200, 400, 600],
+    512: [2, 128, 256, 512, 1200, 1400],
+}
+CASES = [(n, h) for n, hops in HOPS.items() for h in hops]
+
+
+def W(n_fft: int, hop: int) -> Workload:
+    return Workload(name="choice", B=2, T=40 * hop + n_fft + 123, in_dtype="f32", out_dtype="f32", sr=16000,
+                    n_fft=n_fft, hop=hop, win_length=n_fft, n_mels=40 if n_fft < 256 else 64, f_min=0.0,
+                    f_max=8000.0, power=2.0, mel_scale="htk", norm=None, recipe="normal", seed=n_fft + hop)
+
+
+@pytest.mark.parametrize("n_fft,hop", CASES, ids=lambda v: str(v))
+def test_even_hop_each_kernel(n_fft, hop):
+    w = W(n_fft, hop)
+    x = make_input(w)
+    check_close(run_gpu(w, x), oracle_for(w, x), "f32", f"n_fft={n_fft} hop={hop}")
+
+
+@pytest.mark.parametrize("n_fft", sorted(HOPS))
+def test_both_kernels_chosen(n_fft):
+    shapes = {}
+    for hop in HOPS[n_fft]:
+        plan = plan_for(W(n_fft, hop))
+        try:
+            shapes[hop] = fb.fm_plan_get_info(plan)["threads_per_block"]
+        finally:
+            fb.fm_plan_destroy(plan)
+    # the shortest hop runs the packed kernel, the longest the one-frame one
+    assert shapes[HOPS[n_fft][0]] != shapes[HOPS[n_fft][-1]], shapes
