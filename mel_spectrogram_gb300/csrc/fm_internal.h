@@ -217,7 +217,7 @@ struct Variant {
                         // 3: one complex transform per frame pair
   const void* fn;       // __global__ void(KernelParams)
   int hop;              // > 0: compiled for this hop only; else kEvenHops, kOddHops or kAnyHop
-  int groups;           // kind 1: independent tile groups per CTA (one CTA per SM); else 0
+  int groups;           // kind 1: independent tile groups per CTA; else 0
 };
 
 // Variant::hop values other than a compiled-in hop

@@ -639,9 +639,9 @@ __device__ __forceinline__ void consume_x2(const KernelParams& prm, unsigned cha
   }
 }
 
-// One CTA per SM: GR tile groups of P x 16 threads, each running its own tile
-// loop on its own exchange buffer, and one producer warp that stages all their
-// tiles; the tables are shared.
+// GR tile groups of P x 16 threads, each running its own tile loop on its own
+// exchange buffer, and one producer warp that stages all their tiles; the
+// tables are shared. As many CTAs per SM as fit (one at n_fft 256-512).
 template <int N, int P, int Q, int GR, int HOP>
 __global__ void __launch_bounds__(GR* P* kX2Lanes + 32 * kX2ProducerWarps, 1)
     mel_kernel_x2(const __grid_constant__ KernelParams prm) {

@@ -3,9 +3,11 @@
 The packed two-frame kernel (n_fft 64 to 512) keeps one exchange buffer and
 one staged tile per tile group. Once a long hop's staged tile no longer fits,
 the plan takes the one-frame kernel of the same size instead; torchaudio's
-default hop at n_fft 400 (win_length // 2 = 200) is such a hop. Every case
-checks every output element against the float64 oracle, and each size is
-shown to run both kernels over its hop list (their CTA sizes differ)."""
+default hop at n_fft 400 (win_length // 2 = 200) is such a hop. At n_fft 64
+and 128 the packed kernel runs one group per CTA and takes every hop listed.
+Every case checks every output element against the float64 oracle, and the
+sizes with a fallback are shown to run both kernels over their hop lists
+(their CTA sizes differ)."""
 from __future__ import annotations
 
 import pytest
@@ -24,11 +26,12 @@ def _built():
     build()
 
 
-# per size: short hops, n_fft/4, n_fft/2, n_fft, and hops past the packed
-# kernel's staging room that the one-frame kernel still takes
+# per size: short hops, n_fft/4, n_fft/2, n_fft, and long hops (past the
+# packed kernel's staging room at 256-512, where the one-frame kernel takes
+# them; on the packed kernel at 64 and 128)
 HOPS = {
-    64: [2, 16, 32, 64, 600, 800],
-    128: [2, 32, 64, 128, 500, 800],
+    64: [2, 16, 32, 64, 600, 1200],
+    128: [2, 32, 64, 128, 500, 1200],
     256: [2, 64, 128, 256, 500, 700],
     400: [2, 100, 160, 200, 400, 600],
     512: [2, 128, 256, 512, 1200, 1400],
@@ -49,7 +52,7 @@ def test_even_hop_each_kernel(n_fft, hop):
     check_close(run_gpu(w, x), oracle_for(w, x), "f32", f"n_fft={n_fft} hop={hop}")
 
 
-@pytest.mark.parametrize("n_fft", sorted(HOPS))
+@pytest.mark.parametrize("n_fft", [256, 400, 512])
 def test_both_kernels_chosen(n_fft):
     shapes = {}
     for hop in HOPS[n_fft]:
