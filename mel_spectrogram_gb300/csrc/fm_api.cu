@@ -26,7 +26,7 @@ extern const Variant kVariant64, kVariant128, kVariant256, kVariant400, kVariant
 extern const Variant kVariant256one, kVariant400one;
 extern const Variant kVariant64odd, kVariant128odd, kVariant256odd, kVariant400odd, kVariant512odd,
     kVariant1024odd, kVariant2048odd;
-extern const Variant kVariant400c2c;
+extern const Variant kVariant400c2c, kVariant400h160x2h;
 
 // The kernels for (n_fft, hop), in order: a build for exactly this hop if
 // there is one, then those for its parity (even hops stage and read aligned
@@ -45,8 +45,10 @@ const Variant* find_variant(int n_fft, int hop, const Variant* after) {
   if (after == nullptr && n_fft == 400 && even) {
     const char* k = std::getenv("FM_MEL_N400_KERNEL");
     if (k != nullptr && std::strcmp(k, "c2c") == 0) return &kVariant400c2c;
+    if (k != nullptr && std::strcmp(k, "x2h") == 0 && hop == 160) return &kVariant400h160x2h;
   }
-  bool skip = after != nullptr && after != &kVariant400c2c;  // up to and including `after`
+  // up to and including `after` (a diagnostic choice falls back to the list)
+  bool skip = after != nullptr && after != &kVariant400c2c && after != &kVariant400h160x2h;
   for (const Variant* v : all) {
     if (skip) {
       skip = v != after;

@@ -57,16 +57,20 @@ def run_checked(w: Workload, x: np.ndarray, center=True, pad_mode="reflect", pad
 
 
 CASES = [
-    # two-frame kernel: the hop-160 build, any even hop, 256 and 64
+    # two-frame kernel: the hop-160 build, any even hop, 256 and 64; the Q = P
+    # split at 128 (one group per CTA) and 512 (two groups)
     dict(n_fft=400, hop=160, T=16000, n_mels=128, B=3),
     dict(n_fft=400, hop=160, T=201),  # the shortest signal reflect padding allows
     dict(n_fft=400, hop=160, T=200037, B=4, n_mels=128),  # signals' first / last tiles swapped into spare slots
     dict(n_fft=400, hop=100, T=5001, in_dtype="i16", recipe="pcm16"),
     dict(n_fft=256, hop=64, T=6001, mel_scale="slaney", norm="slaney"),
     dict(n_fft=64, hop=16, T=3001, n_mels=40),
-    # one frame per thread
     dict(n_fft=128, hop=32, T=4001),
     dict(n_fft=512, hop=128, T=9001, n_mels=128),
+    dict(n_fft=512, hop=64, T=20001, n_mels=128, B=3, power=1.0, out_dtype="f16"),
+    # one frame per thread: the even-hop fallbacks of the packed sizes, 1024, 2048
+    dict(n_fft=400, hop=200, T=12001, n_mels=128),
+    dict(n_fft=256, hop=500, T=20001),
     dict(n_fft=1024, hop=256, T=9001, in_dtype="f16", recipe="music16"),
     dict(n_fft=2048, hop=512, T=12345, out_dtype="f16", power=1.0),
     # odd hops (contiguous staging)

@@ -10,6 +10,8 @@ sizes with a fallback are shown to run both kernels over their hop lists
 (their CTA sizes differ)."""
 from __future__ import annotations
 
+import dataclasses
+
 import pytest
 
 from mel_spectrogram_gb300 import _binding as fb
@@ -63,3 +65,17 @@ def test_both_kernels_chosen(n_fft):
             fb.fm_plan_destroy(plan)
     # the shortest hop runs the packed kernel, the longest the one-frame one
     assert shapes[HOPS[n_fft][0]] != shapes[HOPS[n_fft][-1]], shapes
+
+
+# the packed kernel's Q = P split (128, 512) and a one-frame fallback (400 at
+# hop 200) under every power mode, 16-bit input and f16 output
+MODES = [dict(power=1.0), dict(power=0.5, out_dtype="f16"), dict(power=2.0, in_dtype="i16", recipe="pcm16"),
+         dict(power=3.0, in_dtype="f16", recipe="music16")]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: "-".join(f"{a}{b}" for a, b in m.items() if a != "recipe"))
+@pytest.mark.parametrize("n_fft,hop", [(128, 32), (512, 128), (400, 200)], ids=lambda v: str(v))
+def test_power_modes_and_dtypes(n_fft, hop, mode):
+    w = dataclasses.replace(W(n_fft, hop), **mode)
+    x = make_input(w)
+    check_close(run_gpu(w, x), oracle_for(w, x), w.out_dtype, f"n_fft={n_fft} hop={hop} {mode}")
