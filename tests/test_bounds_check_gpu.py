@@ -68,9 +68,12 @@ CASES = [
     dict(n_fft=128, hop=32, T=4001),
     dict(n_fft=512, hop=128, T=9001, n_mels=128),
     dict(n_fft=512, hop=64, T=20001, n_mels=128, B=3, power=1.0, out_dtype="f16"),
-    # one frame per thread: the even-hop fallbacks of the packed sizes, 1024, 2048
+    # long even hops: the packed kernel with two groups (400) and one (256),
+    # and the one-frame kernel past that (512)
     dict(n_fft=400, hop=200, T=12001, n_mels=128),
-    dict(n_fft=256, hop=500, T=20001),
+    dict(n_fft=256, hop=700, T=30001),
+    dict(n_fft=512, hop=1400, T=60001),
+    # one frame per thread: 1024, 2048
     dict(n_fft=1024, hop=256, T=9001, in_dtype="f16", recipe="music16"),
     dict(n_fft=2048, hop=512, T=12345, out_dtype="f16", power=1.0),
     # odd hops (contiguous staging)

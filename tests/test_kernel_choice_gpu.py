@@ -1,13 +1,14 @@
-"""Even hops on both sides of the packed kernel's shared-memory limit.
+"""Even hops on both sides of the packed kernel's shared-memory limits.
 
 The packed two-frame kernel (n_fft 64 to 512) keeps one exchange buffer and
-one staged tile per tile group. Once a long hop's staged tile no longer fits,
-the plan takes the one-frame kernel of the same size instead; torchaudio's
+one staged tile per tile group. Once a long hop's staged tile no longer fits
+three groups (n_fft 256, 400) or two (512), the plan takes a build with fewer
+groups per CTA, and past that (512) the one-frame kernel; torchaudio's
 default hop at n_fft 400 (win_length // 2 = 200) is such a hop. At n_fft 64
 and 128 the packed kernel runs one group per CTA and takes every hop listed.
 Every case checks every output element against the float64 oracle, and the
-sizes with a fallback are shown to run both kernels over their hop lists
-(their CTA sizes differ)."""
+sizes with longer-hop builds are shown to run more than one over their hop
+lists (their CTA sizes differ)."""
 from __future__ import annotations
 
 import dataclasses
@@ -29,8 +30,8 @@ def _built():
 
 
 # per size: short hops, n_fft/4, n_fft/2, n_fft, and long hops (past the
-# packed kernel's staging room at 256-512, where the one-frame kernel takes
-# them; on the packed kernel at 64 and 128)
+# three-group packed kernel's staging room at 256-512; on the one-group
+# packed kernel at 64 and 128)
 HOPS = {
     64: [2, 16, 32, 64, 600, 1200],
     128: [2, 32, 64, 128, 500, 1200],
@@ -55,7 +56,7 @@ def test_even_hop_each_kernel(n_fft, hop):
 
 
 @pytest.mark.parametrize("n_fft", [256, 400, 512])
-def test_both_kernels_chosen(n_fft):
+def test_long_hop_builds_chosen(n_fft):
     shapes = {}
     for hop in HOPS[n_fft]:
         plan = plan_for(W(n_fft, hop))
@@ -63,11 +64,11 @@ def test_both_kernels_chosen(n_fft):
             shapes[hop] = fb.fm_plan_get_info(plan)["threads_per_block"]
         finally:
             fb.fm_plan_destroy(plan)
-    # the shortest hop runs the packed kernel, the longest the one-frame one
+    # the shortest hop runs the full packed kernel, the longest a build for long hops
     assert shapes[HOPS[n_fft][0]] != shapes[HOPS[n_fft][-1]], shapes
 
 
-# the packed kernel's Q = P split (128, 512) and a one-frame fallback (400 at
+# the packed kernel's Q = P split (128, 512) and its two-group build (400 at
 # hop 200) under every power mode, 16-bit input and f16 output
 MODES = [dict(power=1.0), dict(power=0.5, out_dtype="f16"), dict(power=2.0, in_dtype="i16", recipe="pcm16"),
          dict(power=3.0, in_dtype="f16", recipe="music16")]
