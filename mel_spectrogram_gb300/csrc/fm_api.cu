@@ -366,10 +366,12 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   // one tile's span fits beside the transform buffer
   int big_span = 0;
   if (var->kind == 2) {
-    const size_t st_bytes = fm::big_staging_bytes(n_fft, hop, in_esize);
-    if (fm::big_span(n_fft, hop) < (1 << 24) && smem_total + st_bytes <= dyn_max) {
-      big_span = (int)fm::big_span(n_fft, hop);
-      smem_total += st_bytes;
+    // one staging buffer per tile group
+    const int F = var->frames_per_tile, GB = var->groups > 0 ? var->groups : 1;
+    const size_t st_bytes = fm::big_staging_bytes(F, n_fft, hop, in_esize);
+    if (fm::big_span(F, n_fft, hop) < (1 << 24) && smem_total + GB * st_bytes <= dyn_max) {
+      big_span = (int)fm::big_span(F, n_fft, hop);
+      smem_total += GB * st_bytes;
     }
   }
   // allow the device maximum once, so plans of different sizes never undercut each other

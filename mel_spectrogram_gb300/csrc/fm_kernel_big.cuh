@@ -19,9 +19,12 @@
 //   split  : X[k], X[M-k] from Z[k], Z[M-k] and W_N^k, |X|^p into a power
 //            tile that aliases the buffer;
 //   mel    : the CSR projection, lane = frame.
-// F = 32768 / n_fft (8, 4, 2): a tile is 16 K complex values, 139 KB of
-// shared memory with one float2 of padding per 16 (strided accesses spread
-// over the banks). Twiddles (float64-built tables) and the window are read
+// A CTA holds 16 K complex values (32768 / n_fft frames), 139 KB of shared
+// memory with one float2 of padding per 16 (strided accesses spread over the
+// banks). With GB tile groups the CTA's threads and buffer split into GB
+// groups that run their own tiles (32768 / n_fft / GB frames) on their own
+// named barrier, sharing the twiddle rows and the filterbank; GB = 1 is one
+// group of the whole CTA. Twiddles (float64-built tables) and the window are read
 // from global memory through the read-only cache.
 #pragma once
 
@@ -77,14 +80,20 @@ __host__ __device__ inline BigLayout big_layout(int n_fft, int n_mels, int nnz) 
   return L;
 }
 
-// Samples one tile's frames cover, (F - 1) hop + n_fft: the span the kernel
-// prefetches into a staging buffer after the tables when it fits
-// (KernelParams::big_span), 16-byte aligned.
-__host__ __device__ constexpr long long big_span(int n_fft, int hop) {
-  return (long long)(big_frames(n_fft) - 1) * hop + n_fft;
+// Samples a tile of F frames covers, (F - 1) hop + n_fft: the span the kernel
+// prefetches into a staging buffer (one per group) after the tables when it
+// fits (KernelParams::big_span), 16-byte aligned.
+__host__ __device__ constexpr long long big_span(int F, int n_fft, int hop) {
+  return (long long)(F - 1) * hop + n_fft;
 }
-__host__ __device__ constexpr size_t big_staging_bytes(int n_fft, int hop, int esize) {
-  return (size_t)((big_span(n_fft, hop) * esize + 15) / 16 * 16);
+__host__ __device__ constexpr size_t big_staging_bytes(int F, int n_fft, int hop, int esize) {
+  return (size_t)((big_span(F, n_fft, hop) * esize + 15) / 16 * 16);
+}
+// barrier over one tile group of n threads: the CTA barrier when the group is
+// the whole CTA, else named barrier `id`
+__device__ __forceinline__ void big_sync(int id, int n) {
+  if (n == kBigThreads) __syncthreads();
+  else asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 __device__ __forceinline__ int big_phys(int i) { return i + (i >> 4); }
 
@@ -106,18 +115,18 @@ __device__ __forceinline__ float big_sample(const Raw* __restrict__ sig, long lo
 // Every global load of the tile is issued before the first one is used (the
 // loop has a compile-time trip count), so the tile waits for one memory
 // latency rather than one per few pairs.
-template <int N, typename Raw>
+template <int N, int F, int TH, typename Raw>
 __device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ sig, long long T, long long s0,
                                          int hop, const float2* __restrict__ win2, const PadSpec& ps, int tid,
                                          Cap x_cap) {
-  constexpr int M = N / 2, F = big_frames(N), FS = big_frame_stride(M);
-  constexpr int PER = F * M / kBigThreads;
-  static_assert((F * M) % kBigThreads == 0, "pairs must divide evenly over the threads");
+  constexpr int M = N / 2, FS = big_frame_stride(M);
+  constexpr int PER = F * M / TH;
+  static_assert((F * M) % TH == 0, "pairs must divide evenly over the threads");
   const bool interior = s0 >= 0 && s0 + (long long)(F - 1) * hop + N <= T;
   float2 v[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
+    const int idx = tid + i * TH, f = idx / M, n = idx % M;
     const long long s = s0 + (long long)f * hop + 2 * n;
     if (interior) {
       v[i] = FM_IN(s >= 0 && s + 1 < T, x_cap.err) ? make_float2(raw_to_float(sig[s]), raw_to_float(sig[s + 1]))
@@ -128,7 +137,7 @@ __device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ si
   }
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
+    const int idx = tid + i * TH, f = idx / M, n = idx % M;
     const float2 w = __ldg(win2 + n);
     put(s_x, 0, f * FS + big_phys(n), make_float2(v[i].x * w.x, v[i].y * w.y), x_cap);
   }
@@ -136,14 +145,14 @@ __device__ __forceinline__ void big_load(float2* s_x, const Raw* __restrict__ si
 
 // The same from a staging buffer that holds the tile's padded samples
 // (st[i] = the sample at padded position s0 + i, see stage_run).
-template <int N, typename Raw>
+template <int N, int F, int TH, typename Raw>
 __device__ __forceinline__ void big_load_staged(float2* s_x, const Raw* st, int hop, const float2* __restrict__ win2,
                                                 int tid, Cap x_cap, Cap st_cap) {
-  constexpr int M = N / 2, F = big_frames(N), FS = big_frame_stride(M);
-  constexpr int PER = F * M / kBigThreads;
+  constexpr int M = N / 2, FS = big_frame_stride(M);
+  constexpr int PER = F * M / TH;
 #pragma unroll 8
   for (int i = 0; i < PER; ++i) {
-    const int idx = tid + i * kBigThreads, f = idx / M, n = idx % M;
+    const int idx = tid + i * TH, f = idx / M, n = idx % M;
     const Raw* p = st + f * hop + 2 * n;
     const float2 w = __ldg(win2 + n);
     const float2 v = FM_IN(f * hop + 2 * n + 1 < st_cap.n, st_cap.err) ? make_float2(raw_to_float(p[0]), raw_to_float(p[1]))
@@ -160,16 +169,16 @@ __device__ __forceinline__ float2 big_tw(const float2* s_tw, int t) {
   return cmul(s_tw[t & (kBigTwFine - 1)], s_tw[kBigTwFine + (t >> 6)]);
 }
 
-template <int M, int F, int R, int NS>
-__device__ __forceinline__ void big_pass(float2* s_x, const float2* s_tw, int tid, Cap x_cap) {
+template <int M, int F, int TH, int R, int NS>
+__device__ __forceinline__ void big_pass(float2* s_x, const float2* s_tw, int tid, int bar, Cap x_cap) {
   constexpr int J = M / R;  // butterflies per frame
   constexpr int FS = big_frame_stride(M);
-  static_assert((F * J) % kBigThreads == 0, "butterflies must divide evenly over the threads");
-  constexpr int TASKS = F * J / kBigThreads;
+  static_assert((F * J) % TH == 0, "butterflies must divide evenly over the threads");
+  constexpr int TASKS = F * J / TH;
   float2 v[TASKS][R];
 #pragma unroll
   for (int t = 0; t < TASKS; ++t) {
-    const int task = tid + t * kBigThreads;
+    const int task = tid + t * TH;
     const int f = task / J, j = task % J;
     const float2* xf = s_x + f * FS;
 #pragma unroll
@@ -181,31 +190,31 @@ __device__ __forceinline__ void big_pass(float2* s_x, const float2* s_tw, int ti
     }
     dft<R>(v[t]);
   }
-  __syncthreads();  // every read of this pass before any write
+  big_sync(bar, TH);  // every read of this pass before any write
 #pragma unroll
   for (int t = 0; t < TASKS; ++t) {
-    const int task = tid + t * kBigThreads;
+    const int task = tid + t * TH;
     const int f = task / J, j = task % J;
     float2* xf = s_x + f * FS;
     const int d = (j / NS) * NS * R + (j % NS);
 #pragma unroll
     for (int r = 0; r < R; ++r) put(xf, f * FS, big_phys(d + r * NS), v[t][r], x_cap);
   }
-  __syncthreads();
+  big_sync(bar, TH);
 }
 
 // Real-FFT split and |X|^p for k = 0 .. M/2 of every frame, into the power
 // tile (float rows of M + 1, aliasing the buffer: all reads, barrier, writes).
-template <int M, int F, int MODE>
-__device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2* s_twn, float pw, int tid,
+template <int M, int F, int TH, int MODE>
+__device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2* s_twn, float pw, int tid, int bar,
                                           Cap x_cap, Cap p_cap) {
   constexpr int FS = big_frame_stride(M), PS = M + 1;
   constexpr int PAIRS = M / 2 + 1, TOTAL = F * PAIRS;
-  constexpr int PER = (TOTAL + kBigThreads - 1) / kBigThreads;
+  constexpr int PER = (TOTAL + TH - 1) / TH;
   float lo[PER], hi[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int task = tid + i * kBigThreads;
+    const int task = tid + i * TH;
     lo[i] = hi[i] = 0.0f;
     if (task < TOTAL) {
       const int f = task / PAIRS, k = task % PAIRS;
@@ -216,75 +225,79 @@ __device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2
       split_pair<MODE>(zk, zm, w, pw, lo[i], hi[i]);
     }
   }
-  __syncthreads();
+  big_sync(bar, TH);
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int task = tid + i * kBigThreads;
+    const int task = tid + i * TH;
     if (task < TOTAL) {
       const int f = task / PAIRS, k = task % PAIRS;
       put(s_pw, 0, f * PS + k, lo[i], p_cap);
       put(s_pw, 0, f * PS + M - k, hi[i], p_cap);
     }
   }
-  __syncthreads();
+  big_sync(bar, TH);
 }
 
-template <int N, typename Raw>
-__device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned char* smem) {
-  constexpr int M = N / 2, F = big_frames(N), NWARPS = kBigThreads / 32;
+// The tile loop of group grp (tid: the thread within the group): tiles
+// blockIdx.x + gridDim.x * (grp + GB k) of F = 32768 / n_fft / GB frames, on
+// the group's share of the transform buffer and its named barrier 1 + grp.
+template <int N, int GB, typename Raw>
+__device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned char* smem, int grp, int tid) {
+  constexpr int M = N / 2, F = big_frames(N) / GB, TH = kBigThreads / GB, NWARPS = TH / 32;
   constexpr int R0 = BigRadices<M>::R0, R1 = BigRadices<M>::R1, R2 = BigRadices<M>::R2;
-  static_assert(R0 * R1 * R2 == M, "radices must multiply to M");
-  float2* s_x = reinterpret_cast<float2*>(smem);
-  float* s_pw = reinterpret_cast<float*>(smem);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  static_assert(R0 * R1 * R2 == M && F * GB == big_frames(N) && TH % 32 == 0, "radices, frames and groups");
+  float2* s_x = reinterpret_cast<float2*>(smem) + (size_t)grp * F * big_frame_stride(M);
+  float* s_pw = reinterpret_cast<float*>(s_x);
+  const int warp = tid >> 5, lane = tid & 31, bar = 1 + grp;
   const Raw* in = static_cast<const Raw*>(prm.in);
   const float2* win2 = reinterpret_cast<const float2*>(prm.win);
   const long long T = prm.T;
   const TileSplitter split(prm.tiles_per_signal);
   const PadSpec pads = {prm.zpad, prm.cpad, prm.pad_mode};
-  // With a staging buffer (prm.big_span > 0), the next tile's samples are
+  // With staging buffers (prm.big_span > 0), the next tile's samples are
   // prefetched by cp.async while this tile's transform runs.
   const BigLayout lay = big_layout(N, prm.n_mels, prm.nnz);
   const float2* s_tw = reinterpret_cast<const float2*>(smem + lay.tw);  // W_M rows, then W_N rows
   const float2* s_twn = s_tw + kBigTwFine + M / kBigTwFine;
   const int4* s_mel = reinterpret_cast<const int4*>(smem + lay.mel);
   const float* s_mw = reinterpret_cast<const float*>(smem + lay.mw);
-  Raw* s_st = reinterpret_cast<Raw*>(smem + lay.st);
   const int span = prm.big_span;
+  Raw* s_st = reinterpret_cast<Raw*>(smem + lay.st + (size_t)grp * ((span * sizeof(Raw) + 15) / 16 * 16));
   // buffer sizes for the debug build's index checks (the staging buffer holds
   // span samples, rounded up to 16 bytes)
   const Cap x_cap = {F * big_frame_stride(M), prm.err}, p_cap = {F * (M + 1), prm.err};
   const Cap st_cap = {span, prm.err};
   const long long out_total = prm.B * (long long)prm.n_mels * prm.n_frames;
+  const long long first = (long long)blockIdx.x + (long long)gridDim.x * grp, stride = (long long)gridDim.x * GB;
   auto prefetch = [&](long long t) {
     long long bb;
     int tq;
     split(t, bb, tq);
-    stage_run<Raw>(in + bb * T, T, (long long)tq * F * prm.hop - prm.lead, span, s_st, tid, kBigThreads, pads,
-                   st_cap);
+    stage_run<Raw>(in + bb * T, T, (long long)tq * F * prm.hop - prm.lead, span, s_st, tid, TH, pads, st_cap);
     cp_async_commit();
   };
-  if (span > 0 && (long long)blockIdx.x < prm.total_tiles) prefetch(blockIdx.x);
-  for (long long tile = blockIdx.x; tile < prm.total_tiles; tile += gridDim.x) {
+  if (span > 0 && first < prm.total_tiles) prefetch(first);
+  for (long long tile = first; tile < prm.total_tiles; tile += stride) {
     long long b;
     int tt;
     split(tile, b, tt);
     const int t0 = tt * F;
     if (span > 0) cp_async_wait_all();  // this thread's copies of the tile have landed
-    __syncthreads();  // the previous tile's mel reads are done; the staged tile is visible
+    big_sync(bar, TH);  // the previous tile's mel reads are done; the staged tile is visible
     if (span > 0)
-      big_load_staged<N, Raw>(s_x, s_st, prm.hop, win2, tid, x_cap, st_cap);
+      big_load_staged<N, F, TH, Raw>(s_x, s_st, prm.hop, win2, tid, x_cap, st_cap);
     else
-      big_load<N, Raw>(s_x, in + b * T, T, (long long)t0 * prm.hop - prm.lead, prm.hop, win2, pads, tid, x_cap);
-    __syncthreads();
-    if (span > 0 && tile + gridDim.x < prm.total_tiles) prefetch(tile + gridDim.x);  // staging read: reuse it
-    big_pass<M, F, R0, 1>(s_x, s_tw, tid, x_cap);
-    big_pass<M, F, R1, R0>(s_x, s_tw, tid, x_cap);
-    big_pass<M, F, R2, R0 * R1>(s_x, s_tw, tid, x_cap);
+      big_load<N, F, TH, Raw>(s_x, in + b * T, T, (long long)t0 * prm.hop - prm.lead, prm.hop, win2, pads, tid,
+                              x_cap);
+    big_sync(bar, TH);
+    if (span > 0 && tile + stride < prm.total_tiles) prefetch(tile + stride);  // staging read: reuse it
+    big_pass<M, F, TH, R0, 1>(s_x, s_tw, tid, bar, x_cap);
+    big_pass<M, F, TH, R1, R0>(s_x, s_tw, tid, bar, x_cap);
+    big_pass<M, F, TH, R2, R0 * R1>(s_x, s_tw, tid, bar, x_cap);
     switch (prm.power_mode) {
-      case 0: big_split<M, F, 0>(s_x, s_pw, s_twn, prm.power, tid, x_cap, p_cap); break;
-      case 1: big_split<M, F, 1>(s_x, s_pw, s_twn, prm.power, tid, x_cap, p_cap); break;
-      default: big_split<M, F, 2>(s_x, s_pw, s_twn, prm.power, tid, x_cap, p_cap); break;
+      case 0: big_split<M, F, TH, 0>(s_x, s_pw, s_twn, prm.power, tid, bar, x_cap, p_cap); break;
+      case 1: big_split<M, F, TH, 1>(s_x, s_pw, s_twn, prm.power, tid, bar, x_cap, p_cap); break;
+      default: big_split<M, F, TH, 2>(s_x, s_pw, s_twn, prm.power, tid, bar, x_cap, p_cap); break;
     }
     const int n_valid = min(F, prm.n_frames - t0);
     const long long obase = b * prm.n_mels * (long long)prm.n_frames + t0;
@@ -298,7 +311,7 @@ __device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned 
   cp_async_wait_all();  // nothing stays in flight past the end of the CTA
 }
 
-template <int N>
+template <int N, int GB>
 __global__ void __launch_bounds__(kBigThreads, 1) mel_kernel_big(const KernelParams prm) {
   constexpr int M = N / 2, ROWS = M / kBigTwFine;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -321,18 +334,21 @@ __global__ void __launch_bounds__(kBigThreads, 1) mel_kernel_big(const KernelPar
   cp_async_commit();
   cp_async_wait_all();
   pdl_wait();  // caller buffers only after the previous kernel in the stream is done
-  // (the first barrier of the tile loop publishes the tables)
-  if (prm.in_dtype == FM_F32) run_tiles_big<N, float>(prm, smem);
-  else if (prm.in_dtype == FM_I16) run_tiles_big<N, short>(prm, smem);
-  else run_tiles_big<N, __half>(prm, smem);
+  __syncthreads();  // the tables are visible to every group
+  constexpr int TH = kBigThreads / GB;
+  const int grp = GB == 1 ? 0 : __shfl_sync(0xffffffffu, tid / TH, 0), gtid = tid % TH;
+  if (prm.in_dtype == FM_F32) run_tiles_big<N, GB, float>(prm, smem, grp, gtid);
+  else if (prm.in_dtype == FM_I16) run_tiles_big<N, GB, short>(prm, smem, grp, gtid);
+  else run_tiles_big<N, GB, __half>(prm, smem, grp, gtid);
 }
 
 }  // namespace fm
 
-// Instantiate one large-transform variant: FM_DEFINE_VARIANT_BIG(name, N)
-#define FM_DEFINE_VARIANT_BIG(NAME, N)                                                               \
-  namespace fm {                                                                                     \
-  template __global__ void mel_kernel_big<N>(const KernelParams);                                   \
-  extern const Variant NAME = {N, 0, 0, big_frames(N), kBigThreads, 0, 2,                            \
-                               (const void*)&mel_kernel_big<N>, kAnyHop};                            \
+// Instantiate one large-transform variant: FM_DEFINE_VARIANT_BIG(name, N, GB),
+// GB tile groups per CTA
+#define FM_DEFINE_VARIANT_BIG(NAME, N, GB)                                                            \
+  namespace fm {                                                                                      \
+  template __global__ void mel_kernel_big<N, GB>(const KernelParams);                                \
+  extern const Variant NAME = {N, 0, 0, big_frames(N) / GB, kBigThreads, 0, 2,                        \
+                               (const void*)&mel_kernel_big<N, GB>, kAnyHop, GB};                     \
   }
