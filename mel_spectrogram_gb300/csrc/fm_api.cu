@@ -27,6 +27,7 @@ extern const Variant kVariant256g2, kVariant256g1, kVariant400g2, kVariant400g1,
 extern const Variant kVariant64odd, kVariant128odd, kVariant256odd, kVariant400odd, kVariant512odd,
     kVariant1024odd, kVariant2048odd;
 extern const Variant kVariant400c2c, kVariant400h160x2h;
+extern const Variant kVariant400h100, kVariant400h200, kVariant128h32, kVariant256h64, kVariant512h128;
 
 // The kernels for (n_fft, hop), in order: a build for exactly this hop if
 // there is one, then those for its parity (even hops stage and read aligned
@@ -34,12 +35,14 @@ extern const Variant kVariant400c2c, kVariant400h160x2h;
 // for longer hops, ahead of the one-frame kernel; odd hops take the generic
 // kernel's contiguous staging), then one for any hop.
 const Variant* find_variant(int n_fft, int hop, const Variant* after) {
-  static const Variant* all[] = {&kVariant400h160, &kVariant64,      &kVariant128,     &kVariant256,
-                                 &kVariant256g2,   &kVariant256g1,   &kVariant400,     &kVariant400g2,
-                                 &kVariant400g1,   &kVariant512x2,   &kVariant512g1,   &kVariant512,
-                                 &kVariant1024,    &kVariant2048,    &kVariant4096,    &kVariant8192,
-                                 &kVariant16384,   &kVariant64odd,   &kVariant128odd,  &kVariant256odd,
-                                 &kVariant400odd,  &kVariant512odd,  &kVariant1024odd, &kVariant2048odd};
+  static const Variant* all[] = {&kVariant400h160, &kVariant400h100, &kVariant400h200, &kVariant128h32,
+                                 &kVariant256h64,  &kVariant512h128, &kVariant64,      &kVariant128,
+                                 &kVariant256,     &kVariant256g2,   &kVariant256g1,   &kVariant400,
+                                 &kVariant400g2,   &kVariant400g1,   &kVariant512x2,   &kVariant512g1,
+                                 &kVariant512,     &kVariant1024,    &kVariant2048,    &kVariant4096,
+                                 &kVariant8192,    &kVariant16384,   &kVariant64odd,   &kVariant128odd,
+                                 &kVariant256odd,  &kVariant400odd,  &kVariant512odd,  &kVariant1024odd,
+                                 &kVariant2048odd};
   const bool even = hop % 2 == 0;
   // diagnostic A/B switch: the paired-frame complex transform at n_fft 400
   // (even hops) instead of the two-frame packed kernel
