@@ -68,14 +68,17 @@ def test_long_hop_builds_chosen(n_fft):
     assert shapes[HOPS[n_fft][0]] != shapes[HOPS[n_fft][-1]], shapes
 
 
-# the packed kernel's Q = P split (128, 512) and its two-group build (400 at
-# hop 200) under every power mode, 16-bit input and f16 output
+# the packed kernel's Q = P split (128, 512), its hop-specialised builds
+# (128 / 32, 256 / 64, 400 / 100, 512 / 128, 400 / 200 with two groups) and
+# an any-hop build (400 / 120) under every power mode, 16-bit input and f16
+# output
 MODES = [dict(power=1.0), dict(power=0.5, out_dtype="f16"), dict(power=2.0, in_dtype="i16", recipe="pcm16"),
          dict(power=3.0, in_dtype="f16", recipe="music16")]
 
 
 @pytest.mark.parametrize("mode", MODES, ids=lambda m: "-".join(f"{a}{b}" for a, b in m.items() if a != "recipe"))
-@pytest.mark.parametrize("n_fft,hop", [(128, 32), (512, 128), (400, 200)], ids=lambda v: str(v))
+@pytest.mark.parametrize("n_fft,hop", [(128, 32), (256, 64), (400, 100), (512, 128), (400, 200), (400, 120)],
+                         ids=lambda v: str(v))
 def test_power_modes_and_dtypes(n_fft, hop, mode):
     w = dataclasses.replace(W(n_fft, hop), **mode)
     x = make_input(w)
