@@ -77,7 +77,10 @@ typedef enum { FM_NORMALIZED_NONE = 0, FM_NORMALIZED_WINDOW = 1, FM_NORMALIZED_F
  *   n_fft      : DFT size. Supported: 400 and the powers of two 64 .. 16384
  *                (README "Usage": "400 or a power of 2 in [64, 16384]").
  *   hop        : frame advance in samples, > 0 (odd hops run a kernel that
- *                stages each tile as one contiguous run of samples).
+ *                stages each tile as one contiguous run of samples; the plan
+ *                takes the first kernel for its n_fft and hop whose staged
+ *                tiles fit shared memory, so long hops run builds with fewer
+ *                tiles in flight per CTA).
  *   win_length : Hann length, 1 .. n_fft; 0 means n_fft.
  *   n_mels     : number of mel filters, 1 .. 256.
  *   f_min      : lowest filter edge in Hz, >= 0.
