@@ -28,12 +28,15 @@ extern const Variant kVariant64odd, kVariant128odd, kVariant256odd, kVariant400o
     kVariant1024odd, kVariant2048odd;
 extern const Variant kVariant400c2c, kVariant400h160x2h;
 extern const Variant kVariant400h100, kVariant400h200, kVariant128h32, kVariant256h64, kVariant512h128;
+extern const Variant kVariant1024big, kVariant2048big;
 
 // The kernels for (n_fft, hop), in order: a build for exactly this hop if
 // there is one, then those for its parity (even hops stage and read aligned
 // sample pairs: the packed two-frame kernel, with fewer tile groups per CTA
 // for longer hops, ahead of the one-frame kernel; odd hops take the generic
-// kernel's contiguous staging), then one for any hop.
+// kernel's contiguous staging), then one for any hop (the large-transform
+// kernel, last at n_fft 1024 and 2048, where it takes the hops the others
+// have no shared memory for).
 const Variant* find_variant(int n_fft, int hop, const Variant* after) {
   static const Variant* all[] = {&kVariant400h160, &kVariant400h100, &kVariant400h200, &kVariant128h32,
                                  &kVariant256h64,  &kVariant512h128, &kVariant64,      &kVariant128,
@@ -42,7 +45,7 @@ const Variant* find_variant(int n_fft, int hop, const Variant* after) {
                                  &kVariant512,     &kVariant1024,    &kVariant2048,    &kVariant4096,
                                  &kVariant8192,    &kVariant16384,   &kVariant64odd,   &kVariant128odd,
                                  &kVariant256odd,  &kVariant400odd,  &kVariant512odd,  &kVariant1024odd,
-                                 &kVariant2048odd};
+                                 &kVariant2048odd, &kVariant1024big, &kVariant2048big};
   const bool even = hop % 2 == 0;
   // diagnostic A/B switch: the paired-frame complex transform at n_fft 400
   // (even hops) instead of the two-frame packed kernel

@@ -1,4 +1,5 @@
-// Mel kernel for the large transforms (n_fft = 4096, 8192, 16384; sm_103a).
+// Mel kernel for the large transforms (n_fft = 4096, 8192, 16384; sm_103a),
+// and for n_fft 1024 and 2048 at hops too long for the one-frame kernel.
 //
 // Same path as the other kernels (padding and framing as index arithmetic,
 // periodic Hann, real DFT through the complex M = n_fft/2 point DFT of
@@ -37,6 +38,14 @@ constexpr int kBigThreads = 512;
 // Radices of the three autosorting passes, M = R0 R1 R2.
 template <int M>
 struct BigRadices;
+template <>
+struct BigRadices<512> {
+  static constexpr int R0 = 8, R1 = 8, R2 = 8;
+};
+template <>
+struct BigRadices<1024> {
+  static constexpr int R0 = 16, R1 = 16, R2 = 4;
+};
 template <>
 struct BigRadices<2048> {
   static constexpr int R0 = 16, R1 = 16, R2 = 8;

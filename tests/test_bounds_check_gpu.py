@@ -73,6 +73,9 @@ CASES = [
     dict(n_fft=400, hop=200, T=12001, n_mels=128),
     dict(n_fft=256, hop=700, T=30001),
     dict(n_fft=512, hop=1400, T=60001),
+    # the large-transform kernel at hops too long for the one-frame kernel
+    dict(n_fft=2048, hop=1024, T=30001, n_mels=128),
+    dict(n_fft=1024, hop=2600, T=40001, in_dtype="i16", recipe="pcm16"),
     # one frame per thread: 1024, 2048
     dict(n_fft=1024, hop=256, T=9001, in_dtype="f16", recipe="music16"),
     dict(n_fft=2048, hop=512, T=12345, out_dtype="f16", power=1.0),

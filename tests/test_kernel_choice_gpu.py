@@ -4,11 +4,15 @@ The packed two-frame kernel (n_fft 64 to 512) keeps one exchange buffer and
 one staged tile per tile group. Once a long hop's staged tile no longer fits
 three groups (n_fft 256, 400) or two (512), the plan takes a build with fewer
 groups per CTA, and past that (512) the one-frame kernel; torchaudio's
-default hop at n_fft 400 (win_length // 2 = 200) is such a hop. At n_fft 64
+default hop at n_fft 400 (win_length // 2 = 200) is such a hop. At n_fft
+1024 and 2048 the one-frame kernel's staged tile stops fitting at long hops
+(2048 from ~810 on, half-overlap hop 1024 among them) and the
+large-transform kernel, which reads frames straight from the signal, takes
+them. At n_fft 64
 and 128 the packed kernel runs one group per CTA and takes every hop listed.
 Every case checks every output element against the float64 oracle, and the
 sizes with longer-hop builds are shown to run more than one over their hop
-lists (their CTA sizes differ)."""
+lists (their CTA or tile sizes differ)."""
 from __future__ import annotations
 
 import dataclasses
@@ -38,6 +42,8 @@ HOPS = {
     256: [2, 64, 128, 256, 500, 700],
     400: [2, 100, 160, 200, 400, 600],
     512: [2, 128, 256, 512, 1200, 1400],
+    1024: [2, 256, 512, 2600],
+    2048: [2, 512, 1024, 2048, 2999],
 }
 CASES = [(n, h) for n, hops in HOPS.items() for h in hops]
 
@@ -55,13 +61,14 @@ def test_even_hop_each_kernel(n_fft, hop):
     check_close(run_gpu(w, x), oracle_for(w, x), "f32", f"n_fft={n_fft} hop={hop}")
 
 
-@pytest.mark.parametrize("n_fft", [256, 400, 512])
+@pytest.mark.parametrize("n_fft", [256, 400, 512, 1024, 2048])
 def test_long_hop_builds_chosen(n_fft):
     shapes = {}
     for hop in HOPS[n_fft]:
         plan = plan_for(W(n_fft, hop))
         try:
-            shapes[hop] = fb.fm_plan_get_info(plan)["threads_per_block"]
+            info = fb.fm_plan_get_info(plan)
+            shapes[hop] = (info["threads_per_block"], info["frames_per_tile"])
         finally:
             fb.fm_plan_destroy(plan)
     # the shortest hop runs the full packed kernel, the longest a build for long hops
