@@ -58,6 +58,8 @@ def oracle_for(w: Workload, x: np.ndarray) -> np.ndarray:
 def check_close(got: np.ndarray, ref: np.ndarray, out_dtype: str, what: str = "") -> float:
     """Assert the tolerance rule; return the worst error / allowed ratio."""
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    if got.size == 0:  # e.g. the finite part of an f16 output that saturates everywhere
+        return 0.0
     assert np.all(np.isfinite(got)), f"{what}: non-finite output (unwritten or overflow)"
     err = np.abs(got - ref)
     if out_dtype == "f32":

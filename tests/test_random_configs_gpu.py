@@ -23,7 +23,7 @@ from tests.gpu_util import check_close, check_close_saturating, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 48
+N_CASES = 96
 SIZES = [64, 128, 256, 400, 512, 1024, 2048, 4096, 8192, 16384]
 MODES = ["reflect", "constant", "replicate", "circular"]
 RECIPE = {"f32": "normal", "i16": "pcm16", "f16": "music16"}
