@@ -29,6 +29,7 @@ extern const Variant kVariant64odd, kVariant128odd, kVariant256odd, kVariant400o
 extern const Variant kVariant400c2c, kVariant400h160x2h;
 extern const Variant kVariant400h100, kVariant400h200, kVariant128h32, kVariant256h64, kVariant512h128;
 extern const Variant kVariant1024big, kVariant2048big;
+extern const Variant kVariant4096dif, kVariant8192dif, kVariant16384dif;
 
 // The kernels for (n_fft, hop), in order: a build for exactly this hop if
 // there is one, then those for its parity (even hops stage and read aligned
@@ -43,19 +44,29 @@ const Variant* find_variant(int n_fft, int hop, const Variant* after) {
                                  &kVariant256,     &kVariant256g2,   &kVariant256g1,   &kVariant400,
                                  &kVariant400g2,   &kVariant400g1,   &kVariant512x2,   &kVariant512g1,
                                  &kVariant512,     &kVariant1024,    &kVariant2048,    &kVariant4096,
-                                 &kVariant8192,    &kVariant16384,   &kVariant64odd,   &kVariant128odd,
+                                 &kVariant8192dif, &kVariant8192,    &kVariant16384dif, &kVariant16384,
+                                 &kVariant64odd,   &kVariant128odd,
                                  &kVariant256odd,  &kVariant400odd,  &kVariant512odd,  &kVariant1024odd,
                                  &kVariant2048odd, &kVariant1024big, &kVariant2048big};
   const bool even = hop % 2 == 0;
-  // diagnostic A/B switch: the paired-frame complex transform at n_fft 400
-  // (even hops) instead of the two-frame packed kernel
+  // diagnostic A/B switches: the paired-frame complex transform at n_fft 400
+  // (even hops) instead of the two-frame packed kernel; the
+  // decimation-in-frequency build of the large-transform kernel at 4096, the
+  // three-pass build at 8192 and 16384
   if (after == nullptr && n_fft == 400 && even) {
     const char* k = std::getenv("FM_MEL_N400_KERNEL");
     if (k != nullptr && std::strcmp(k, "c2c") == 0) return &kVariant400c2c;
     if (k != nullptr && std::strcmp(k, "x2h") == 0 && hop == 160) return &kVariant400h160x2h;
   }
+  if (after == nullptr && (n_fft == 4096 || n_fft == 8192 || n_fft == 16384)) {
+    const char* k = std::getenv("FM_MEL_BIG_KERNEL");
+    if (k != nullptr && std::strcmp(k, "dif") == 0 && n_fft == 4096) return &kVariant4096dif;
+    if (k != nullptr && std::strcmp(k, "passes") == 0 && n_fft != 4096)
+      return n_fft == 8192 ? &kVariant8192 : &kVariant16384;
+  }
   // up to and including `after` (a diagnostic choice falls back to the list)
-  bool skip = after != nullptr && after != &kVariant400c2c && after != &kVariant400h160x2h;
+  bool skip = after != nullptr && after != &kVariant400c2c && after != &kVariant400h160x2h &&
+              after != &kVariant4096dif;
   for (const Variant* v : all) {
     if (skip) {
       skip = v != after;
@@ -103,12 +114,44 @@ struct fm_plan {
   mutable HostPipe pipe;  // streams and events of fm_mel_forward_host
   int x2_slots;         // its mel chunk slots
   int big_span;         // large-transform kernel: samples staged per tile (0: loads from global memory)
+  int mel_taps;         // decimation-in-frequency large-transform kernel: the mel mapping (KernelParams)
   float2* c2c;          // paired-frame kernel: its pass-1 table, then W_400^j (inside dmem)
 };
 
 namespace {
 
 int dtype_size(int dt) { return dt == FM_F32 ? 4 : 2; }
+
+// Mel mapping of the decimation-in-frequency large-transform kernel (16
+// warps, F frames a tile), from the filters' tap counts ml: the estimated
+// critical path of one tile's projection in SM cycles under each mapping,
+// the cheaper one wins. A lane per filter and frame: a warp's filters run
+// side by side, so a warp takes its widest filter's taps, about 33 cycles
+// each; a warp per filter: about 40 cycles per 32 taps plus 440 per filter
+// (its shuffle sum and store in one dependent chain). The constants are
+// fitted on GB300 to n_fft 16384 with 256 filters to 22.05 kHz (a lane per
+// filter 2.5 % faster) and with 128 filters to 8 kHz (a warp per filter 15 %
+// faster). FM_MEL_BIG_MEL=taps or lanes overrides the choice.
+bool choose_mel_taps(const std::vector<int>& ml, int F) {
+  const char* k = std::getenv("FM_MEL_BIG_MEL");
+  if (k != nullptr && std::strcmp(k, "taps") == 0) return true;
+  if (k != nullptr && std::strcmp(k, "lanes") == 0) return false;
+  constexpr int kWarps = fm::kBigThreads / 32;
+  const int n = (int)ml.size(), subs = 32 / F;
+  long long lanes = 0, taps = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    long long tl = 0, tt = 0;
+    for (int base = w * subs; base < n; base += kWarps * subs) {
+      int widest = 0;
+      for (int s = 0; s < subs && base + s < n; ++s) widest = std::max(widest, ml[base + s]);
+      tl += widest;
+    }
+    for (int m = w; m < n; m += kWarps) tt += 40LL * ((ml[m] + 31) / 32) + 440;
+    lanes = std::max(lanes, 33 * tl);
+    taps = std::max(taps, tt);
+  }
+  return taps < lanes;
+}
 
 // Mel schedule of the two-frames-per-thread kernel: four chunk streams per
 // warp (one per quarter-warp). Each filter is padded to an even length
@@ -351,7 +394,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
       continue;
     const size_t need =
         v->kind == 1   ? fm::smem_layout_x2(n_fft, hop, v->hop > 0 ? 2 : 1, slots, in_esize, v->groups).total
-        : v->kind == 2 ? fm::big_layout(n_fft, n_mels, nnz).st
+        : v->kind == 2 ? fm::big_layout(n_fft, n_mels, nnz, v->P > 0).st
         : v->kind == 3 ? fm::smem_layout_c2c(hop, n_mels, nnz, in_esize).total
                        : fm::smem_layout(n_fft, hop, n_mels, nnz, v->frames_per_tile, in_esize, v->in_buffers).total;
     // the kernel's static shared memory comes out of the same per-block limit
@@ -368,10 +411,10 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
     dyn_max = avail;
   }
   if (var == nullptr) return FM_ERR_UNSUPPORTED;
-  // large-transform kernel: a staging buffer for the next tile's samples, when
-  // one tile's span fits beside the transform buffer
+  // three-pass large-transform kernel: a staging buffer for the next tile's
+  // samples, when one tile's span fits beside the transform buffer
   int big_span = 0;
-  if (var->kind == 2) {
+  if (var->kind == 2 && var->P == 0) {
     // one staging buffer per tile group
     const int F = var->frames_per_tile, GB = var->groups > 0 ? var->groups : 1;
     const size_t st_bytes = fm::big_staging_bytes(F, n_fft, hop, in_esize);
@@ -413,6 +456,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   p->nnz = nnz;
   p->x2_slots = x2_slots;
   p->big_span = big_span;
+  p->mel_taps = var->kind == 2 && var->P > 0 ? (int)choose_mel_taps(ml, var->frames_per_tile) : 0;
   p->smem = smem_total;
   p->blocks_per_sm = bps;
   p->num_sms = prop.multiProcessorCount;
@@ -424,7 +468,7 @@ extern "C" fm_status fm_plan_create_ex(fm_plan** out, const fm_plan_params* para
   const int S = var->kind == 1 ? fm::in_row_stride_x2(hop, in_esize) : fm::in_row_stride(hop);
   const float in_scale = in_dtype == FM_I16 ? 1.0f / 32768.0f : 1.0f;  // exact power of two
   std::vector<float4> p1(M);
-  for (int pp = 0; pp < var->P && var->kind != 3; ++pp)  // the paired-frame kernel has its own table
+  for (int pp = 0; pp < var->P && var->kind < 2; ++pp)  // the other kernels have their own tables
     for (int q = 0; q < var->Q; ++q) {
       const int j = 2 * (pp + var->P * q);
       const int off = (j / hop) * S + (j % hop);
@@ -589,6 +633,7 @@ extern "C" fm_status fm_mel_forward(const fm_plan* plan, const void* d_in, int64
   prm.err = plan->err;
   prm.win = plan->win;
   prm.big_span = plan->big_span;
+  prm.mel_taps = plan->mel_taps;
   prm.c2c_tab = plan->c2c;
   prm.c2c_tw = plan->c2c + fm::kC2cN;
 

@@ -64,6 +64,8 @@ struct KernelParams {
   unsigned* err;          // device error word (FM_ERR_KERNEL_TIMEOUT etc.)
   const float* win;       // the n_fft-point window (large-transform kernel only)
   int big_span;           // large-transform kernel: samples staged per tile in shared memory (0: none)
+  int mel_taps;           // decimation-in-frequency large-transform kernel: 1 = a warp per filter with the
+                          // lanes over its taps, 0 = a lane per filter and frame
   const float2* c2c_tab;  // paired-frame kernel: (window, tile offset) per role and step
   const float2* c2c_tw;   // paired-frame kernel: W_400^j, j < 400
   // Packed kernel: when tmap_ok, every signal is described to the TMA unit as
@@ -209,7 +211,8 @@ __host__ __device__ inline SmemLayoutX2 smem_layout_x2(int n_fft, int hop, int k
 // One compiled kernel: a fixed n_fft and its FFT split M = P * Q.
 struct Variant {
   int n_fft;
-  int P, Q;             // pass 1: P roles x Q-point DFTs; pass 2: Q x P-point DFTs
+  int P, Q;             // pass 1: P roles x Q-point DFTs; pass 2: Q x P-point DFTs (kind 2: P = 16, Q = M / 16
+                        // for the decimation-in-frequency build, 0 for the three-pass build)
   int frames_per_tile;  // G: frames per tile = lanes per role
   int threads;          // P * G
   int in_buffers;       // 2: the next tile's input lands while this one computes
@@ -217,7 +220,7 @@ struct Variant {
                         // 3: one complex transform per frame pair
   const void* fn;       // __global__ void(KernelParams)
   int hop;              // > 0: compiled for this hop only; else kEvenHops, kOddHops or kAnyHop
-  int groups;           // kind 1: independent tile groups per CTA; else 0
+  int groups;           // kinds 1 and 2: independent tile groups per CTA; else 0
 };
 
 // Variant::hop values other than a compiled-in hop

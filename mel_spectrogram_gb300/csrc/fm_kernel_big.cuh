@@ -66,6 +66,12 @@ __host__ __device__ constexpr int big_frame_stride(int M) { return M + (M >> 4) 
 __host__ __device__ constexpr size_t big_smem_bytes(int n_fft) {
   return sizeof(float2) * (size_t)big_frames(n_fft) * (size_t)big_frame_stride(n_fft / 2);
 }
+// The decimation-in-frequency build (mel_kernel_bigdif) keeps a tile as 16
+// sub-frames of M/16 values per frame, each with its own padding.
+constexpr int kDifR0 = 16;
+__host__ __device__ constexpr size_t big_dif_smem_bytes(int n_fft) {
+  return sizeof(float2) * (size_t)big_frames(n_fft) * kDifR0 * (size_t)big_frame_stride(n_fft / 2 / kDifR0);
+}
 // Twiddles from shared memory in two levels, W^t = W^(t mod 64) W^(64 floor(t / 64)):
 // rows of 64 fine and M/64 (+1) coarse factors of W_M (the passes) and of W_N
 // (the split), gathered from the plan's full tables when a CTA starts. A full
@@ -79,9 +85,9 @@ __host__ __device__ constexpr int big_tw_count(int M) { return 2 * kBigTwFine + 
 struct BigLayout {
   size_t tw, mel, mw, st;
 };
-__host__ __device__ inline BigLayout big_layout(int n_fft, int n_mels, int nnz) {
+__host__ __device__ inline BigLayout big_layout(int n_fft, int n_mels, int nnz, bool dif = false) {
   BigLayout L;
-  size_t o = big_smem_bytes(n_fft);
+  size_t o = dif ? big_dif_smem_bytes(n_fft) : big_smem_bytes(n_fft);
   L.tw = o;   o = align16(o + sizeof(float2) * big_tw_count(n_fft / 2));
   L.mel = o;  o = align16(o + sizeof(int4) * n_mels);
   L.mw = o;   o = align16(o + sizeof(float) * (nnz > 0 ? nnz : 1));
@@ -99,9 +105,10 @@ __host__ __device__ constexpr size_t big_staging_bytes(int F, int n_fft, int hop
   return (size_t)((big_span(F, n_fft, hop) * esize + 15) / 16 * 16);
 }
 // barrier over one tile group of n threads: the CTA barrier when the group is
-// the whole CTA, else named barrier `id`
+// the whole CTA, a warp barrier when it is one warp, else named barrier `id`
 __device__ __forceinline__ void big_sync(int id, int n) {
   if (n == kBigThreads) __syncthreads();
+  else if (n == 32) __syncwarp();
   else asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 __device__ __forceinline__ int big_phys(int i) { return i + (i >> 4); }
@@ -178,7 +185,9 @@ __device__ __forceinline__ float2 big_tw(const float2* s_tw, int t) {
   return cmul(s_tw[t & (kBigTwFine - 1)], s_tw[kBigTwFine + (t >> 6)]);
 }
 
-template <int M, int F, int TH, int R, int NS>
+// TWS: the rows hold W_{TWS M} (a sub-transform of M points reads W_M^t as
+// W_{TWS M}^{TWS t}).
+template <int M, int F, int TH, int R, int NS, int TWS = 1>
 __device__ __forceinline__ void big_pass(float2* s_x, const float2* s_tw, int tid, int bar, Cap x_cap) {
   constexpr int J = M / R;  // butterflies per frame
   constexpr int FS = big_frame_stride(M);
@@ -195,7 +204,7 @@ __device__ __forceinline__ void big_pass(float2* s_x, const float2* s_tw, int ti
     if constexpr (NS > 1) {
       const int e = (j % NS) * (M / (NS * R));  // W_{Ns R}^{(j mod Ns) r} = W_M^{e r}, e r < M
 #pragma unroll
-      for (int r = 1; r < R; ++r) v[t][r] = cmul(v[t][r], big_tw<M>(s_tw, e * r));
+      for (int r = 1; r < R; ++r) v[t][r] = cmul(v[t][r], big_tw<M>(s_tw, e * r * TWS));
     }
     dft<R>(v[t]);
   }
@@ -245,6 +254,103 @@ __device__ __forceinline__ void big_split(float2* s_x, float* s_pw, const float2
     }
   }
   big_sync(bar, TH);
+}
+
+// Sum over the warp of each of acc[0 .. V-1] (V a power of two <= 32):
+// steps over lane offsets 16, 8, ... first halve the values a lane holds (the
+// lanes with the offset bit set keep the upper half, the others the lower,
+// each adding its partner's copy), then the remaining offsets sum one value.
+// Afterwards lane v (32 / V) holds the sum of acc[v]; V - 1 + 5 - log2(V)
+// shuffles in a chain five deep.
+template <int V>
+__device__ __forceinline__ float warp_sum_each(float (&acc)[V], int lane) {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V a power of two");
+  int o = 16;
+#pragma unroll
+  for (int n = V; n > 1; n >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float give = up ? acc[i] : acc[i + n / 2];
+      const float keep = up ? acc[i + n / 2] : acc[i];
+      acc[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+    }
+  }
+#pragma unroll
+  for (; o >= 1; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+  return acc[0];
+}
+
+// Sparse mel projection with the lanes over a filter's taps: filter m goes to
+// warp m mod NWARPS (filter widths grow with m, so every warp gets a like
+// share of the taps); its taps are read 32 at a time (consecutive bins and
+// weights, no bank conflicts), each lane keeping one partial sum per frame,
+// and warp_sum_each adds them up; lane f (32 / F) stores frame f. The cost of
+// a filter is its ceil(taps / 32) loads plus a shuffle sum, against the
+// widest filter's taps one by one when a lane holds a filter
+// (mel_project_lanes), which is why the plan picks between the two from the
+// filter widths. p_cap, nnz, out_left: as mel_project.
+template <int F, int NWARPS, int PS, typename OutT>
+__device__ __forceinline__ void mel_project_taps(const float* s_pw, const int4* __restrict__ s_mel,
+                                                 const float* __restrict__ s_mw, OutT* out_tile, int n_valid,
+                                                 int n_mels, long long n_frames, int warp, int lane, Cap p_cap,
+                                                 int nnz, long long out_left) {
+  constexpr int L = 32 / F;
+  const int f_out = lane / L;
+  const bool writer = lane % L == 0 && f_out < n_valid;
+  for (int m = warp; m < n_mels; m += NWARPS) {
+    const int4 md = s_mel[m];
+    float acc[F];
+#pragma unroll
+    for (int f = 0; f < F; ++f) acc[f] = 0.0f;
+    for (int j = lane; j < md.y; j += 32) {
+      const float w = FM_IN(md.z + j >= 0 && md.z + j < nnz, p_cap.err) ? s_mw[md.z + j] : 0.0f;
+#pragma unroll
+      for (int f = 0; f < F; ++f) acc[f] = fmaf(w, get(s_pw, 0, f * PS + md.x + j, p_cap), acc[f]);
+    }
+    const float sum = warp_sum_each<F>(acc, lane);
+    if (writer && FM_IN(f_out + (long long)m * n_frames < out_left, p_cap.err))
+      store_out(out_tile + (long long)m * n_frames + f_out, sum);
+  }
+}
+
+// Sparse mel projection with a lane per filter and frame (the mapping of
+// mel_project), its taps read eight ahead into registers and summed into two
+// partial sums, so that the widest filter's lane waits for one shared-memory
+// latency per eight taps rather than per tap.
+template <int G, int NWARPS, int PS, typename OutT>
+__device__ __forceinline__ void mel_project_lanes(const float* s_pw, const int4* __restrict__ s_mel,
+                                                  const float* __restrict__ s_mw, OutT* out_tile, int n_valid,
+                                                  int n_mels, long long n_frames, int warp, int lane, Cap p_cap,
+                                                  int nnz, long long out_left) {
+  constexpr int SUBS = 32 / G;
+  const int gg = lane % G, sub = lane / G;
+  const int poff = gg * PS;
+  const bool valid = gg < n_valid;
+  for (int m = warp * SUBS + sub; m < n_mels; m += NWARPS * SUBS) {
+    const int4 md = s_mel[m];
+    float a0 = 0.0f, a1 = 0.0f;
+    int j = 0;
+    for (; j + 8 <= md.y; j += 8) {
+      float w[8], p[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        w[u] = FM_IN(md.z + j + u >= 0 && md.z + j + u < nnz, p_cap.err) ? s_mw[md.z + j + u] : 0.0f;
+        p[u] = get(s_pw, 0, poff + md.x + j + u, p_cap);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; u += 2) {
+        a0 = fmaf(w[u], p[u], a0);
+        a1 = fmaf(w[u + 1], p[u + 1], a1);
+      }
+    }
+    for (; j < md.y; ++j) {
+      const float w = FM_IN(md.z + j >= 0 && md.z + j < nnz, p_cap.err) ? s_mw[md.z + j] : 0.0f;
+      a0 = fmaf(w, get(s_pw, 0, poff + md.x + j, p_cap), a0);
+    }
+    if (valid && FM_IN(gg + (long long)m * n_frames < out_left, p_cap.err))
+      store_out(out_tile + (long long)m * n_frames + gg, a0 + a1);
+  }
 }
 
 // The tile loop of group grp (tid: the thread within the group): tiles
@@ -320,16 +426,14 @@ __device__ __forceinline__ void run_tiles_big(const KernelParams& prm, unsigned 
   cp_async_wait_all();  // nothing stays in flight past the end of the CTA
 }
 
-template <int N, int GB>
-__global__ void __launch_bounds__(kBigThreads, 1) mel_kernel_big(const KernelParams prm) {
+// The plan's tables, once per CTA (the grid is persistent): the twiddle rows
+// gathered from the full W_M and W_N tables, and the filterbank; then the
+// wait for the previous kernel in the stream and a CTA barrier.
+template <int N>
+__device__ __forceinline__ void big_tables(const KernelParams& prm, unsigned char* smem, const BigLayout& lay,
+                                           int tid) {
   constexpr int M = N / 2, ROWS = M / kBigTwFine;
-  extern __shared__ __align__(16) unsigned char smem[];
-  pdl_launch_dependents();
-  // the plan's tables, once per CTA (the grid is persistent): the twiddle rows
-  // gathered from the full W_M and W_N tables, and the filterbank
-  const BigLayout lay = big_layout(N, prm.n_mels, prm.nnz);
   float2* s_tw = reinterpret_cast<float2*>(smem + lay.tw);
-  const int tid = threadIdx.x;
   for (int i = tid; i < kBigTwFine; i += kBigThreads) {
     s_tw[i] = prm.tw_half[i];                             // W_M^i
     s_tw[kBigTwFine + ROWS + i] = prm.tw_full[i];         // W_N^i
@@ -344,6 +448,14 @@ __global__ void __launch_bounds__(kBigThreads, 1) mel_kernel_big(const KernelPar
   cp_async_wait_all();
   pdl_wait();  // caller buffers only after the previous kernel in the stream is done
   __syncthreads();  // the tables are visible to every group
+}
+
+template <int N, int GB>
+__global__ void __launch_bounds__(kBigThreads, 1) mel_kernel_big(const KernelParams prm) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  pdl_launch_dependents();
+  const int tid = threadIdx.x;
+  big_tables<N>(prm, smem, big_layout(N, prm.n_mels, prm.nnz), tid);
   constexpr int TH = kBigThreads / GB;
   const int grp = GB == 1 ? 0 : __shfl_sync(0xffffffffu, tid / TH, 0), gtid = tid % TH;
   if (prm.in_dtype == FM_F32) run_tiles_big<N, GB, float>(prm, smem, grp, gtid);
