@@ -125,13 +125,16 @@ int dtype_size(int dt) { return dt == FM_F32 ? 4 : 2; }
 // Mel mapping of the decimation-in-frequency large-transform kernel (16
 // warps, F frames a tile), from the filters' tap counts ml: the estimated
 // critical path of one tile's projection in SM cycles under each mapping,
-// the cheaper one wins. A lane per filter and frame: a warp's filters run
-// side by side, so a warp takes its widest filter's taps, about 33 cycles
-// each; a warp per filter: about 40 cycles per 32 taps plus 440 per filter
-// (its shuffle sum and store in one dependent chain). The constants are
-// fitted on GB300 to n_fft 16384 with 256 filters to 22.05 kHz (a lane per
-// filter 2.5 % faster) and with 128 filters to 8 kHz (a warp per filter 15 %
-// faster). FM_MEL_BIG_MEL=taps or lanes overrides the choice.
+// the cheaper one wins. A lane per filter and frame (mel_project_lanes): a
+// warp's filters run side by side, so a warp takes its widest filter's taps,
+// about 33 cycles each; a warp per filter (mel_project_taps): about 40 cycles
+// per 32 taps plus 300 per filter (its shuffle sum and store). Measured on
+// GB300, a warp per filter was the faster mapping on every configuration
+// tried: 272.5 against 281.6 us at n_fft 16384 with 256 filters to 22.05 kHz
+// (16 x 30 s, hop 4096), 69.8 against 86.2 us at 16384 and 69.3 against
+// 70.9 us at 8192 with 128 filters to 8 kHz (32 x 10 s, hop n_fft / 4); with
+// these constants the estimate agrees on all three and leaves the lanes to
+// banks of a few narrow filters. FM_MEL_BIG_MEL=taps or lanes overrides it.
 bool choose_mel_taps(const std::vector<int>& ml, int F) {
   const char* k = std::getenv("FM_MEL_BIG_MEL");
   if (k != nullptr && std::strcmp(k, "taps") == 0) return true;
@@ -146,7 +149,7 @@ bool choose_mel_taps(const std::vector<int>& ml, int F) {
       for (int s = 0; s < subs && base + s < n; ++s) widest = std::max(widest, ml[base + s]);
       tl += widest;
     }
-    for (int m = w; m < n; m += kWarps) tt += 40LL * ((ml[m] + 31) / 32) + 440;
+    for (int m = w; m < n; m += kWarps) tt += 40LL * ((ml[m] + 31) / 32) + 300;
     lanes = std::max(lanes, 33 * tl);
     taps = std::max(taps, tt);
   }
