@@ -35,9 +35,10 @@ extern const Variant kVariant4096dif, kVariant8192dif, kVariant16384dif;
 // there is one, then those for its parity (even hops stage and read aligned
 // sample pairs: the packed two-frame kernel, with fewer tile groups per CTA
 // for longer hops, ahead of the one-frame kernel; odd hops take the generic
-// kernel's contiguous staging), then one for any hop (the large-transform
-// kernel, last at n_fft 1024 and 2048, where it takes the hops the others
-// have no shared memory for).
+// kernel's contiguous staging), then those for any hop (the large-transform
+// kernels: at n_fft 8192 and 16384 the decimation-in-frequency build ahead
+// of the three-pass one; last at 1024 and 2048, where the three-pass build
+// takes the hops the others have no shared memory for).
 const Variant* find_variant(int n_fft, int hop, const Variant* after) {
   static const Variant* all[] = {&kVariant400h160, &kVariant400h100, &kVariant400h200, &kVariant128h32,
                                  &kVariant256h64,  &kVariant512h128, &kVariant64,      &kVariant128,
