@@ -389,3 +389,28 @@ def test_pins_catch_planted_mistake(mutate):
 def test_mutants_do_not_leak():
     assert "oracle_mutant" not in sys.modules or sys.modules["oracle_mutant"] is not real_oracle
     pins.check_bin_centre_cosine(real_oracle)
+
+
+def test_oracle_dft_at_the_large_sizes():
+    """The oracle's DFT at the sizes of the large-transform kernels (4096 to
+    16384, the huge workload's 16384 among them), where an angle 2 pi k n / N
+    formed without reducing k n mod N first would lose digits: Parseval on
+    random rows, and the closed form of a cosine on bin k0, whose one-sided
+    spectrum is N/2 at k0 and zero elsewhere. The bound on the cosine, 1e-13 N,
+    sits between the oracle's own error (3.9e-12 at 16384) and that of the
+    same matrices built from the unreduced angle (1.2e-8). Run on the oracle
+    itself only (each matrix pair is 1 GB at 16384, too heavy for the
+    planted-mistake loop)."""
+    rng = np.random.default_rng(16384)
+    for N in (4096, 8192, 16384):
+        y = rng.standard_normal((2, N))
+        n = np.arange(N)
+        k0 = N // 2 - 7 if N == 16384 else 3 * N // 8 + 5
+        c = np.cos(2.0 * math.pi * ((k0 * n) % N) / N)
+        X = real_oracle.dft_onesided(np.vstack([y, c[None, :]]))
+        e = np.abs(X[:2]) ** 2
+        lhs = e[:, 0] + 2.0 * e[:, 1 : N // 2].sum(axis=1) + e[:, N // 2]
+        assert np.allclose(lhs, N * (y * y).sum(axis=1), rtol=1e-11), N
+        expect = np.zeros(N // 2 + 1)
+        expect[k0] = N / 2
+        assert np.abs(X[2] - expect).max() <= 1e-13 * N, (N, np.abs(X[2] - expect).max())
